@@ -15,9 +15,9 @@ Workloads (dims follow the fused small-batch decode layer of a DeepSeek-style Mo
 model; the pages describe MXFP8 attention/shared weights with 32x32 E8M0 scales and
 MXFP4 routed experts with 1x32 scales):
 
-* ``tiny``        hidden 256, 4 q heads x 64, one KV latent of 64, window 16 over 32
-                  cached tokens in 16-token pages, 8 experts top-2, intermediate 128,
-                  1 row.
+* ``tiny``        hidden 256, 4 q heads x 64, one KV latent of 64, q/o ranks 128, window
+                  16 over 32 cached tokens in 16-token pages, 8 experts top-2,
+                  intermediate 128, 1 row.
 * ``small_r11``   a mid-size case spanning several kernel tiles with ragged edges:
                   11 rows over 3 requests (one pad row).
 * ``full_r1``     hidden 4096, 64 q heads x 128, KV latent 512, causal window 128,
@@ -36,7 +36,7 @@ import torch
 # Layer dimensions.  q_rank / o_rank are not given on the pages; 1024 makes one full
 # layer weigh about 0.9 GB, which is the per-layer size the workloads quote.
 # --------------------------------------------------------------------------------------
-_TINY = dict(hidden=256, n_q_heads=4, head_dim=64, kv_dim=64, q_rank=64, o_rank=64,
+_TINY = dict(hidden=256, n_q_heads=4, head_dim=64, kv_dim=64, q_rank=128, o_rank=128,
              n_experts=8, topk=2, moe_inter=128, shared_inter=128,
              window=16, swa_width=16, causal=1, block_size=16, kv_record_bytes=80,
              eps=1e-6, swiglu_clamp=7.0, routed_scale=1.0)

@@ -1,0 +1,83 @@
+// Instantiations and launcher of the MX block-scaled GEMM (mx_gemm.cuh).
+#include "kernels.h"
+
+namespace mono {
+
+namespace {
+
+// Ring depth per variant: two CTAs fit on one SM in every case.
+template <int FMT, int NT>
+struct Stages;
+template <> struct Stages<8, 1> { static constexpr int value = 8; };
+template <> struct Stages<8, 2> { static constexpr int value = 8; };
+template <> struct Stages<8, 4> { static constexpr int value = 6; };
+template <> struct Stages<8, 6> { static constexpr int value = 4; };
+template <> struct Stages<4, 2> { static constexpr int value = 5; };
+
+template <int FMT, int NT>
+constexpr int smem_of() {
+  return GemmLayout<FMT, NT, Stages<FMT, NT>::value>::BYTES;
+}
+
+template <int FMT, int NT>
+void* kernel_of() {
+  return reinterpret_cast<void*>(&mx_gemm_kernel<FMT, NT, Stages<FMT, NT>::value>);
+}
+
+void* variant_kernel(GemmVariant v, int* smem) {
+  if (v.fmt == 8) {
+    switch (v.nt) {
+      case 1: *smem = smem_of<8, 1>(); return kernel_of<8, 1>();
+      case 2: *smem = smem_of<8, 2>(); return kernel_of<8, 2>();
+      case 4: *smem = smem_of<8, 4>(); return kernel_of<8, 4>();
+      case 6: *smem = smem_of<8, 6>(); return kernel_of<8, 6>();
+      default: return nullptr;
+    }
+  }
+  if (v.fmt == 4 && v.nt == 2) {
+    *smem = smem_of<4, 2>();
+    return kernel_of<4, 2>();
+  }
+  return nullptr;
+}
+
+}  // namespace
+
+int gemm_smem_bytes(GemmVariant v) {
+  int s = 0;
+  return variant_kernel(v, &s) ? s : -1;
+}
+
+cudaError_t gemm_prepare(GemmVariant v) {
+  int smem = 0;
+  void* k = variant_kernel(v, &smem);
+  if (!k) return cudaErrorInvalidValue;
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+int gemm_ctas_per_sm(GemmVariant v) {
+  int smem = 0, n = 0;
+  void* k = variant_kernel(v, &smem);
+  if (!k) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, GEMM_THREADS, smem) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+cudaError_t launch_gemm(const Launch& L, GemmVariant v, const CUtensorMap& map,
+                        const GemmParams& p, int grid) {
+  int smem = 0;
+  if (!variant_kernel(v, &smem)) return cudaErrorInvalidValue;
+  const dim3 g(grid), b(GEMM_THREADS);
+  if (v.fmt == 8) {
+    switch (v.nt) {
+      case 1: return launch_ex(L, g, b, smem, mx_gemm_kernel<8, 1, Stages<8, 1>::value>, map, p);
+      case 2: return launch_ex(L, g, b, smem, mx_gemm_kernel<8, 2, Stages<8, 2>::value>, map, p);
+      case 4: return launch_ex(L, g, b, smem, mx_gemm_kernel<8, 4, Stages<8, 4>::value>, map, p);
+      default: return launch_ex(L, g, b, smem, mx_gemm_kernel<8, 6, Stages<8, 6>::value>, map, p);
+    }
+  }
+  return launch_ex(L, g, b, smem, mx_gemm_kernel<4, 2, Stages<4, 2>::value>, map, p);
+}
+
+}  // namespace mono

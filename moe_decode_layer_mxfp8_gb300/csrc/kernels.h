@@ -1,0 +1,125 @@
+// Internal launch interface between the host API (mono_layer.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "mx_gemm.cuh"
+
+namespace mono {
+
+// Launch helper: every kernel of the step is launched with programmatic stream
+// serialisation so that it may be scheduled while its predecessor drains; each kernel
+// calls griddepcontrol.wait before it touches anything the predecessor wrote.
+struct Launch {
+  cudaStream_t stream;
+  bool pdl;
+};
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(const Launch& L, dim3 grid, dim3 block, size_t smem,
+                             void (*kern)(KArgs...), Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = L.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+struct NormArgs {
+  const __nv_bfloat16* in;
+  int in_ld;
+  const __nv_bfloat16* gamma;
+  int dim;
+  float eps;
+  __half* out;
+  int out_ld;
+};
+
+struct QkvNormInsertArgs {
+  const __nv_bfloat16* qkv;  // [rows, q_rank + kv_dim]
+  int q_rank, kv_dim;
+  const __nv_bfloat16 *gq, *gkv;
+  float eps;
+  __half* qlatn;             // [rows, q_rank]
+  __nv_bfloat16* kvn;        // [rows, kv_dim]
+  const int *positions, *row_req, *block_table;
+  int max_blocks, n_req, block_size;
+  uint8_t* cache;
+  long long stride_block, stride_tok, num_blocks;
+  int* status;
+};
+
+struct AttnArgs {
+  const __nv_bfloat16* q;  // [rows, n_q * head_dim]
+  __half* o;               // [rows, n_q * head_dim]
+  const int *positions, *row_req, *block_table;
+  int rows, max_blocks, n_req, block_size;
+  int n_q, kv_dim, window, swa_width, causal;
+  const uint8_t* cache;
+  long long stride_block, stride_tok, num_blocks;
+  int splits;
+  float* part;   // [rows, n_q, splits, head_dim + 2]
+  int* counters; // [rows, kv_dim / head_dim], left at zero
+  int* status;
+};
+
+struct RouterArgs {
+  const __half* u;  // [rows, H]
+  const float* wr;  // [E, H]
+  int rows, E, H;
+  float* logits;    // [rows, E]
+};
+
+struct TopkArgs {
+  const float* logits;
+  const int* positions;
+  int rows, E, k;
+  float routed_scale;
+  int* topk_idx;
+  float* topk_w;
+  int* slot_pos;  // [rows, k] expert-sorted position of (row, slot)
+  int* perm;      // [rows * k] sorted position -> row
+  RouteInfo* route;
+  int* user_idx;
+  float* user_w;
+  int* status;
+};
+
+struct FinalArgs {
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* h;
+  const float* ys;
+  const float* yr;
+  const int* slot_pos;
+  const float* topk_w;
+  const int* positions;
+  int rows, H, k;
+  __nv_bfloat16* out;
+};
+
+cudaError_t launch_rmsnorm(const Launch&, const NormArgs&, int rows);
+cudaError_t launch_qkv_norm_insert(const Launch&, const QkvNormInsertArgs&, int rows);
+cudaError_t launch_attention(const Launch&, const AttnArgs&, int head_dim, int groups);
+cudaError_t attention_prepare(int head_dim);  // raises the dynamic shared-memory limit
+cudaError_t launch_router(const Launch&, const RouterArgs&);
+cudaError_t launch_topk(const Launch&, const TopkArgs&);
+cudaError_t launch_final(const Launch&, const FinalArgs&);
+
+// MX GEMM variants: fmt 8 (MXFP8) with nt in {1, 2, 4, 6}; fmt 4 (MXFP4) with nt 2.
+struct GemmVariant {
+  int fmt, nt;
+};
+int gemm_smem_bytes(GemmVariant v);
+cudaError_t gemm_prepare(GemmVariant v);  // raises the dynamic shared-memory limit
+int gemm_ctas_per_sm(GemmVariant v);
+cudaError_t launch_gemm(const Launch&, GemmVariant v, const CUtensorMap& map, const GemmParams& p,
+                        int grid);
+
+}  // namespace mono

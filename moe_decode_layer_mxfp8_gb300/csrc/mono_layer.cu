@@ -1,0 +1,513 @@
+// Host side of the C ABI (include/mono_layer.h): validation, tensor maps, the scratch arena
+// and the launch schedule of one layer step.
+//
+// Schedule (stream order, each launch programmatically serialised on its predecessor):
+//   K1  rmsnorm(x) -> wqkv -> q/kv norm + KV insert -> wq_b
+//   K2  split-window attention (+ combine) -> wo_a -> wo_b + residual -> rmsnorm(h)
+//       -> router -> top-k + grouping -> shared gate_up/SwiGLU -> shared down
+//       -> routed gate_up/SwiGLU -> routed down -> final combine
+// ("Mono decode layer for DeepSeek-V4.1-Flash on MI355X", launch table K1 and K2; the
+// pages' in-kernel tensor-parallel all-reduces have no counterpart on one GPU.)
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "../../include/mono_layer.h"
+#include "kernels.h"
+
+using namespace mono;
+
+namespace {
+
+constexpr int kLaunchesPerStep = 15;
+
+enum DenseId { D_WQKV = 0, D_WQB, D_WOA, D_WOB, D_SHGU, D_SHD, D_COUNT };
+
+struct DensePlan {
+  CUtensorMap map;
+  const uint8_t* scales;
+  int N, K, n_tiles, ksplit, swiglu_I;
+  int* counters;
+};
+
+}  // namespace
+
+struct mono_layer {
+  mono_layer_spec spec;
+  mono_layer_weights w;
+  int device = 0, num_sms = 0;
+  uint8_t* arena = nullptr;
+  size_t arena_bytes = 0;
+  size_t buf_off[MONO_BUF_COUNT] = {};
+  size_t buf_bytes[MONO_BUF_COUNT] = {};
+  float* ws = nullptr;         // split-K partial tiles
+  int* counters = nullptr;     // split-K counters of every dense plan, then attention counters
+  int* attn_counters = nullptr;
+  float* attn_part = nullptr;
+  int* status = nullptr;
+  RouteInfo* route = nullptr;
+  int* perm = nullptr;
+  DensePlan dense[D_COUNT];
+  CUtensorMap map_ex_gu, map_ex_d;
+  int ctas_gemm8[7] = {};  // by nt
+  int ctas_gemm4 = 0;
+  int attn_min_splits = 1;
+  template <class T>
+  T* buf(int which) const {
+    return reinterpret_cast<T*>(arena + buf_off[which]);
+  }
+};
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool get_encoder() {
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// 2D byte tensor [rows, row_bytes] with 32-row x 128-byte boxes and 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, long long rows, long long row_bytes) {
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {BOX_BYTES, BOX_ROWS};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int check_spec(const mono_layer_spec& s) {
+  const int qw = s.n_q_heads * s.head_dim;
+  if (s.hidden <= 0 || s.n_q_heads <= 0 || s.q_rank <= 0 || s.o_rank <= 0 || s.kv_dim <= 0 ||
+      s.moe_inter <= 0 || s.shared_inter <= 0 || s.n_experts <= 0 || s.block_size <= 0)
+    return MONO_ERR_UNSUPPORTED_DIMS;
+  // reduction lengths are whole 128-element stages
+  if (s.hidden % 128 || s.q_rank % 128 || s.o_rank % 128 || qw % 128 || s.moe_inter % 128 ||
+      s.shared_inter % 128)
+    return MONO_ERR_UNSUPPORTED_DIMS;
+  if (s.kv_dim % 32 || s.kv_dim > 1024) return MONO_ERR_UNSUPPORTED_DIMS;
+  if (s.head_dim != 64 && s.head_dim != 128) return MONO_ERR_UNSUPPORTED_DIMS;
+  if (s.kv_dim % s.head_dim) return MONO_ERR_UNSUPPORTED_DIMS;
+  const int G = s.kv_dim / s.head_dim;
+  if (s.n_q_heads % G || s.n_q_heads / G > 16) return MONO_ERR_UNSUPPORTED_DIMS;
+  if (s.topk < 1 || s.topk > 8 || s.topk > s.n_experts || s.n_experts > MAX_EXPERTS)
+    return MONO_ERR_UNSUPPORTED_DIMS;
+  if (s.window < 1 || s.window > 1024 || s.swa_width < 1 || s.swa_width > 1024)
+    return MONO_ERR_UNSUPPORTED_DIMS;
+  if (s.kv_record_bytes < s.kv_dim + 4 || s.kv_record_bytes % 16) return MONO_ERR_UNSUPPORTED_DIMS;
+  if (s.max_rows < 1 || s.max_rows > 48) return MONO_ERR_TOO_MANY_ROWS;
+  return MONO_OK;
+}
+
+int nt_bucket(int rows) {
+  const int t = (rows + 7) / 8;
+  return t <= 1 ? 1 : t <= 2 ? 2 : t <= 4 ? 4 : 6;
+}
+
+int cuda_fail(cudaError_t e) {
+  (void)cudaGetLastError();
+  return e == cudaErrorMemoryAllocation ? MONO_ERR_OUT_OF_MEMORY : MONO_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mono_layer_strerror(int code) {
+  switch (code) {
+    case MONO_OK: return "ok";
+    case MONO_ERR_INVALID_ARG: return "invalid argument";
+    case MONO_ERR_UNSUPPORTED_DIMS: return "unsupported layer dimensions";
+    case MONO_ERR_TOO_MANY_ROWS: return "too many rows";
+    case MONO_ERR_BAD_ALIGNMENT: return "pointer or stride not 16-byte aligned";
+    case MONO_ERR_BAD_KV_VIEW: return "KV-cache view strides overlap records or pages";
+    case MONO_ERR_UNSUPPORTED_DEVICE: return "not an sm_103 (GB300) device";
+    case MONO_ERR_CUDA: return "CUDA runtime error";
+    case MONO_ERR_OUT_OF_MEMORY: return "out of device memory";
+    case MONO_ERR_DEVICE_STATUS: return "device status word raised";
+    default: return "unknown error";
+  }
+}
+
+int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, mono_layer_t** out) {
+  if (!spec || !wt || !out) return MONO_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = check_spec(*spec);
+  if (rc) return rc;
+  const void* ptrs[] = {wt->attn_norm, wt->q_norm, wt->kv_norm, wt->ffn_norm, wt->wqkv, wt->wqkv_s,
+                        wt->wq_b,      wt->wq_b_s,   wt->wo_a,   wt->wo_a_s,    wt->wo_b, wt->wo_b_s,
+                        wt->router,    wt->sh_gu,    wt->sh_gu_s, wt->sh_d,     wt->sh_d_s, wt->ex_gu,
+                        wt->ex_gu_s,   wt->ex_d,     wt->ex_d_s};
+  for (const void* p : ptrs) {
+    if (!p) return MONO_ERR_INVALID_ARG;
+    if (!aligned16(p)) return MONO_ERR_BAD_ALIGNMENT;
+  }
+  int dev = 0;
+  cudaDeviceProp prop;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MONO_ERR_CUDA;
+  }
+  if (prop.major != 10 || prop.minor != 3) return MONO_ERR_UNSUPPORTED_DEVICE;
+  if (!get_encoder()) return MONO_ERR_CUDA;
+
+  mono_layer* h = new (std::nothrow) mono_layer();
+  if (!h) return MONO_ERR_OUT_OF_MEMORY;
+  h->spec = *spec;
+  h->w = *wt;
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+  const mono_layer_spec& s = h->spec;
+  const int R = s.max_rows, H = s.hidden, E = s.n_experts, K = s.topk;
+  const int QW = s.n_q_heads * s.head_dim, A = s.q_rank + s.kv_dim;
+  const int G = s.kv_dim / s.head_dim;
+
+  // dense GEMV plans: K split until the tiles cover the SMs
+  struct Def {
+    const uint8_t *w, *sc;
+    int N, K, swiglu;
+  } defs[D_COUNT] = {{wt->wqkv, wt->wqkv_s, A, H, 0},
+                     {wt->wq_b, wt->wq_b_s, QW, s.q_rank, 0},
+                     {wt->wo_a, wt->wo_a_s, s.o_rank, QW, 0},
+                     {wt->wo_b, wt->wo_b_s, H, s.o_rank, 0},
+                     {wt->sh_gu, wt->sh_gu_s, 2 * s.shared_inter, H, s.shared_inter},
+                     {wt->sh_d, wt->sh_d_s, H, s.shared_inter, 0}};
+  size_t ws_floats = 0;
+  int total_tiles = 0;
+  for (int i = 0; i < D_COUNT; ++i) {
+    DensePlan& d = h->dense[i];
+    d.scales = defs[i].sc;
+    d.N = defs[i].N;
+    d.K = defs[i].K;
+    d.swiglu_I = defs[i].swiglu;
+    d.n_tiles = d.swiglu_I ? d.swiglu_I / BOX_ROWS : (d.N + TILE_M - 1) / TILE_M;
+    const int chunks = d.K / 128;
+    d.ksplit = 1;
+    while (d.n_tiles * d.ksplit < h->num_sms && d.ksplit * 2 <= chunks) d.ksplit *= 2;
+    ws_floats = std::max(ws_floats, (size_t)d.n_tiles * d.ksplit * TILE_M * 48);
+    total_tiles += d.n_tiles;
+    if (!make_map(&d.map, defs[i].w, d.N, d.K)) {
+      delete h;
+      return MONO_ERR_CUDA;
+    }
+  }
+  if (!make_map(&h->map_ex_gu, wt->ex_gu, (long long)E * 2 * s.moe_inter, H / 2) ||
+      !make_map(&h->map_ex_d, wt->ex_d, (long long)E * H, s.moe_inter / 2)) {
+    delete h;
+    return MONO_ERR_CUDA;
+  }
+  const int width = std::max(s.causal ? s.window : s.swa_width, s.window);
+  h->attn_min_splits = (width + 127) / 128;
+  const int attn_splits_max = std::max(8, h->attn_min_splits);
+
+  // scratch arena
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) / 256 * 256;
+    return o;
+  };
+  const size_t sizes[MONO_BUF_COUNT] = {
+      (size_t)R * H * 2,  (size_t)R * A * 2,      (size_t)R * s.q_rank * 2, (size_t)R * s.kv_dim * 2,
+      (size_t)R * QW * 2, (size_t)R * QW * 2,     (size_t)R * s.o_rank * 2, (size_t)R * H * 2,
+      (size_t)R * H * 2,  (size_t)R * E * 4,      (size_t)R * K * 4,        (size_t)R * K * 4,
+      (size_t)R * K * 4,  (size_t)R * s.shared_inter * 2, (size_t)R * H * 4,
+      (size_t)R * K * s.moe_inter * 2, (size_t)R * K * H * 4};
+  for (int b = 0; b < MONO_BUF_COUNT; ++b) {
+    h->buf_bytes[b] = sizes[b];
+    h->buf_off[b] = take(sizes[b]);
+  }
+  const size_t o_ws = take(ws_floats * 4);
+  const size_t o_ctr = take((size_t)(total_tiles + R * G) * 4);
+  const size_t o_part = take((size_t)R * s.n_q_heads * attn_splits_max * (s.head_dim + 2) * 4);
+  const size_t o_status = take(16);
+  const size_t o_route = take(sizeof(RouteInfo));
+  const size_t o_perm = take((size_t)R * K * 4);
+  h->arena_bytes = off;
+  cudaError_t e = cudaMalloc(&h->arena, h->arena_bytes);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e);
+  }
+  e = cudaMemset(h->arena, 0, h->arena_bytes);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(h->arena);
+    delete h;
+    return cuda_fail(e);
+  }
+  h->ws = reinterpret_cast<float*>(h->arena + o_ws);
+  h->counters = reinterpret_cast<int*>(h->arena + o_ctr);
+  int* c = h->counters;
+  for (int i = 0; i < D_COUNT; ++i) {
+    h->dense[i].counters = c;
+    c += h->dense[i].n_tiles;
+  }
+  h->attn_counters = c;
+  h->attn_part = reinterpret_cast<float*>(h->arena + o_part);
+  h->status = reinterpret_cast<int*>(h->arena + o_status);
+  h->route = reinterpret_cast<RouteInfo*>(h->arena + o_route);
+  h->perm = reinterpret_cast<int*>(h->arena + o_perm);
+
+  // kernel attributes and occupancy
+  for (int nt : {1, 2, 4, 6}) {
+    if (gemm_prepare({8, nt}) != cudaSuccess) rc = MONO_ERR_CUDA;
+    h->ctas_gemm8[nt] = std::max(1, gemm_ctas_per_sm({8, nt}));
+  }
+  if (gemm_prepare({4, 2}) != cudaSuccess) rc = MONO_ERR_CUDA;
+  h->ctas_gemm4 = std::max(1, gemm_ctas_per_sm({4, 2}));
+  if (attention_prepare(s.head_dim) != cudaSuccess) rc = MONO_ERR_CUDA;
+  if (rc) {
+    (void)cudaGetLastError();
+    cudaFree(h->arena);
+    delete h;
+    return rc;
+  }
+  *out = h;
+  return MONO_OK;
+}
+
+void mono_layer_free(mono_layer_t* h) {
+  if (!h) return;
+  if (h->arena) cudaFree(h->arena);
+  delete h;
+}
+
+int mono_layer_status(mono_layer_t* h, int clear) {
+  if (!h) return MONO_ERR_INVALID_ARG;
+  int v = 0;
+  cudaError_t e = cudaMemcpy(&v, h->status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && clear) e = cudaMemset(h->status, 0, sizeof(int));
+  if (e == cudaSuccess && clear) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return v;
+}
+
+int mono_layer_buffer(mono_layer_t* h, int which, void** dev_ptr, size_t* bytes) {
+  if (!h || which < 0 || which >= MONO_BUF_COUNT) return MONO_ERR_INVALID_ARG;
+  if (dev_ptr) *dev_ptr = h->arena + h->buf_off[which];
+  if (bytes) *bytes = h->buf_bytes[which];
+  return MONO_OK;
+}
+
+int mono_layer_read_buffer(mono_layer_t* h, int which, void* host_dst, size_t bytes) {
+  if (!h || which < 0 || which >= MONO_BUF_COUNT || !host_dst) return MONO_ERR_INVALID_ARG;
+  if (bytes > h->buf_bytes[which]) return MONO_ERR_INVALID_ARG;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess)
+    e = cudaMemcpy(host_dst, h->arena + h->buf_off[which], bytes, cudaMemcpyDeviceToHost);
+  return e == cudaSuccess ? MONO_OK : cuda_fail(e);
+}
+
+int mono_layer_launches_per_step(mono_layer_t* h) { return h ? kLaunchesPerStep : MONO_ERR_INVALID_ARG; }
+
+int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) {
+  if (!h || !a) return MONO_ERR_INVALID_ARG;
+  const mono_layer_spec& s = h->spec;
+  const int R = a->rows;
+  if (R < 1) return MONO_ERR_INVALID_ARG;
+  if (R > s.max_rows) return MONO_ERR_TOO_MANY_ROWS;
+  if (!a->x_in || !a->x_out || !a->positions || !a->row_req || !a->block_table || !a->kv_cache)
+    return MONO_ERR_INVALID_ARG;
+  if (a->max_blocks < 1 || a->n_req < 1 || a->kv_num_blocks < 1) return MONO_ERR_INVALID_ARG;
+  if (!aligned16(a->x_in) || !aligned16(a->x_out) || !aligned16(a->kv_cache) ||
+      a->kv_stride_tok % 16 || a->kv_stride_block % 16)
+    return MONO_ERR_BAD_ALIGNMENT;
+  if (a->kv_stride_tok < s.kv_record_bytes ||
+      a->kv_stride_block < (int64_t)s.block_size * a->kv_stride_tok)
+    return MONO_ERR_BAD_KV_VIEW;
+
+  const Launch L{reinterpret_cast<cudaStream_t>(stream_ptr), true};
+  const int H = s.hidden, E = s.n_experts, K = s.topk, QW = s.n_q_heads * s.head_dim;
+  const int A = s.q_rank + s.kv_dim, G = s.kv_dim / s.head_dim;
+  const int nt = nt_bucket(R);
+  const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(a->x_in);
+  cudaError_t e = cudaSuccess;
+#define RUN(call)                        \
+  do {                                   \
+    e = (call);                          \
+    if (e != cudaSuccess) return cuda_fail(e); \
+  } while (0)
+
+  auto dense = [&](int id, const __half* act, int act_ld, int epi, void* outp, int out_ld,
+                   const __nv_bfloat16* resid) {
+    const DensePlan& d = h->dense[id];
+    GemmParams p = {};
+    p.scales = d.scales;
+    p.scale_ld = d.K / 32;
+    p.K = d.K;
+    p.N = d.N;
+    p.swiglu_I = d.swiglu_I;
+    p.act = act;
+    p.act_ld = act_ld;
+    p.dense_rows = R;
+    p.n_tiles = d.n_tiles;
+    p.ksplit = d.ksplit;
+    p.epi = epi;
+    p.out = outp;
+    p.out_ld = out_ld;
+    p.resid = resid;
+    p.resid_ld = H;
+    p.clamp = s.swiglu_clamp;
+    p.ws = h->ws;
+    p.counters = d.counters;
+    p.status = h->status;
+    const int items = d.n_tiles * d.ksplit;
+    const int grid = std::min(items, h->num_sms * h->ctas_gemm8[nt]);
+    return launch_gemm(L, {8, nt}, d.map, p, grid);
+  };
+  auto expert = [&](const CUtensorMap& map, const uint8_t* sc, int Kdim, int rows_per_mat,
+                    int swiglu, int n_tiles, const __half* act, int act_ld, const int* rowmap,
+                    int epi, void* outp, int out_ld) {
+    GemmParams p = {};
+    p.scales = sc;
+    p.scale_ld = Kdim / 32;
+    p.K = Kdim;
+    p.N = rows_per_mat;
+    p.rows_per_mat = rows_per_mat;
+    p.swiglu_I = swiglu;
+    p.act = act;
+    p.act_ld = act_ld;
+    p.act_rowmap = rowmap;
+    p.n_tiles = n_tiles;
+    p.ksplit = 1;
+    p.route = h->route;
+    p.epi = epi;
+    p.out = outp;
+    p.out_ld = out_ld;
+    p.clamp = s.swiglu_clamp;
+    p.status = h->status;
+    return launch_gemm(L, {4, 2}, map, p, h->num_sms * h->ctas_gemm4);
+  };
+
+  // ---------------------------------------------------------------- K1: attention front
+  RUN(launch_rmsnorm(L, {x, H, (const __nv_bfloat16*)h->w.attn_norm, H, s.eps,
+                         h->buf<__half>(MONO_BUF_XN), H}, R));
+  RUN(dense(D_WQKV, h->buf<__half>(MONO_BUF_XN), H, EPI_BF16, h->buf<void>(MONO_BUF_QKV), A,
+            nullptr));
+  {
+    QkvNormInsertArgs q = {};
+    q.qkv = h->buf<__nv_bfloat16>(MONO_BUF_QKV);
+    q.q_rank = s.q_rank;
+    q.kv_dim = s.kv_dim;
+    q.gq = (const __nv_bfloat16*)h->w.q_norm;
+    q.gkv = (const __nv_bfloat16*)h->w.kv_norm;
+    q.eps = s.eps;
+    q.qlatn = h->buf<__half>(MONO_BUF_QLATN);
+    q.kvn = h->buf<__nv_bfloat16>(MONO_BUF_KVN);
+    q.positions = a->positions;
+    q.row_req = a->row_req;
+    q.block_table = a->block_table;
+    q.max_blocks = a->max_blocks;
+    q.n_req = a->n_req;
+    q.block_size = s.block_size;
+    q.cache = a->kv_cache;
+    q.stride_block = a->kv_stride_block;
+    q.stride_tok = a->kv_stride_tok;
+    q.num_blocks = a->kv_num_blocks;
+    q.status = h->status;
+    RUN(launch_qkv_norm_insert(L, q, R));
+  }
+  RUN(dense(D_WQB, h->buf<__half>(MONO_BUF_QLATN), s.q_rank, EPI_BF16, h->buf<void>(MONO_BUF_Q),
+            QW, nullptr));
+
+  // ---------------------------------------------------------------- K2: attention back
+  {
+    AttnArgs t = {};
+    t.q = h->buf<__nv_bfloat16>(MONO_BUF_Q);
+    t.o = h->buf<__half>(MONO_BUF_O);
+    t.positions = a->positions;
+    t.row_req = a->row_req;
+    t.block_table = a->block_table;
+    t.rows = R;
+    t.max_blocks = a->max_blocks;
+    t.n_req = a->n_req;
+    t.block_size = s.block_size;
+    t.n_q = s.n_q_heads;
+    t.kv_dim = s.kv_dim;
+    t.window = s.window;
+    t.swa_width = s.swa_width;
+    t.causal = s.causal;
+    t.cache = a->kv_cache;
+    t.stride_block = a->kv_stride_block;
+    t.stride_tok = a->kv_stride_tok;
+    t.num_blocks = a->kv_num_blocks;
+    const int want = (2 * h->num_sms + R * G - 1) / (R * G);
+    t.splits = std::max(h->attn_min_splits, std::min(8, want));
+    t.part = h->attn_part;
+    t.counters = h->attn_counters;
+    t.status = h->status;
+    RUN(launch_attention(L, t, s.head_dim, G));
+  }
+  RUN(dense(D_WOA, h->buf<__half>(MONO_BUF_O), QW, EPI_F16, h->buf<void>(MONO_BUF_OA), s.o_rank,
+            nullptr));
+  RUN(dense(D_WOB, h->buf<__half>(MONO_BUF_OA), s.o_rank, EPI_RESID_BF16, h->buf<void>(MONO_BUF_H),
+            H, x));
+
+  // ---------------------------------------------------------------- K2: FFN seam and MoE
+  RUN(launch_rmsnorm(L, {h->buf<__nv_bfloat16>(MONO_BUF_H), H, (const __nv_bfloat16*)h->w.ffn_norm,
+                         H, s.eps, h->buf<__half>(MONO_BUF_U), H}, R));
+  RUN(launch_router(L, {h->buf<__half>(MONO_BUF_U), h->w.router, R, E, H,
+                        h->buf<float>(MONO_BUF_LOGITS)}));
+  {
+    TopkArgs t = {};
+    t.logits = h->buf<float>(MONO_BUF_LOGITS);
+    t.positions = a->positions;
+    t.rows = R;
+    t.E = E;
+    t.k = K;
+    t.routed_scale = s.routed_scale;
+    t.topk_idx = h->buf<int>(MONO_BUF_TOPK_IDX);
+    t.topk_w = h->buf<float>(MONO_BUF_TOPK_W);
+    t.slot_pos = h->buf<int>(MONO_BUF_SLOT_POS);
+    t.perm = h->perm;
+    t.route = h->route;
+    t.user_idx = a->topk_idx_out;
+    t.user_w = a->topk_w_out;
+    t.status = h->status;
+    RUN(launch_topk(L, t));
+  }
+  RUN(dense(D_SHGU, h->buf<__half>(MONO_BUF_U), H, EPI_SWIGLU_F16, h->buf<void>(MONO_BUF_TS),
+            s.shared_inter, nullptr));
+  RUN(dense(D_SHD, h->buf<__half>(MONO_BUF_TS), s.shared_inter, EPI_F32, h->buf<void>(MONO_BUF_YS),
+            H, nullptr));
+  RUN(expert(h->map_ex_gu, h->w.ex_gu_s, H, 2 * s.moe_inter, s.moe_inter, s.moe_inter / BOX_ROWS,
+             h->buf<__half>(MONO_BUF_U), H, h->perm, EPI_SWIGLU_F16, h->buf<void>(MONO_BUF_TR),
+             s.moe_inter));
+  RUN(expert(h->map_ex_d, h->w.ex_d_s, s.moe_inter, H, 0, H / TILE_M, h->buf<__half>(MONO_BUF_TR),
+             s.moe_inter, nullptr, EPI_F32, h->buf<void>(MONO_BUF_YR), H));
+  {
+    FinalArgs f = {};
+    f.x = x;
+    f.h = h->buf<__nv_bfloat16>(MONO_BUF_H);
+    f.ys = h->buf<float>(MONO_BUF_YS);
+    f.yr = h->buf<float>(MONO_BUF_YR);
+    f.slot_pos = h->buf<int>(MONO_BUF_SLOT_POS);
+    f.topk_w = h->buf<float>(MONO_BUF_TOPK_W);
+    f.positions = a->positions;
+    f.rows = R;
+    f.H = H;
+    f.k = K;
+    f.out = reinterpret_cast<__nv_bfloat16*>(a->x_out);
+    RUN(launch_final(L, f));
+  }
+#undef RUN
+  return MONO_OK;
+}
+
+}  // extern "C"

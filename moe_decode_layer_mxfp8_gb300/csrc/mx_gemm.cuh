@@ -1,0 +1,478 @@
+// MX block-scaled skinny GEMM: y[rows, N] = x[rows, K] . W[N, K]^T with W in MXFP8 (e4m3,
+// 32x32 E8M0 blocks) or MXFP4 (e2m1, 1x32 E8M0 blocks), x bf16 (fed to the tensor cores as
+// exact f16 copies), f32 accumulation.  Used for every weight contraction of the layer:
+// wqkv, wq_b, wo_a, wo_b, the shared expert and the routed experts ("Mono decode layer for
+// DeepSeek-V4.1-Flash on MI355X", launch table rows K1 and K2; section Design: weights read
+// in place, MXFP8 row-major with 32x32 E8M0 scales, MXFP4 experts).
+//
+// Work item = 64 weight rows (two 32-row TMA boxes) x a K range x up to NT*8 activation
+// rows.  Dense matrices split K across items and reduce the partial tiles in a fixed order
+// (the last-arriving CTA of a tile sums them), so results are bit-reproducible.  Expert
+// matrices take one item per (expert, 64 rows, 16 routed rows) and the full K.
+//
+// CTA = 1 producer warp + 4 consumer warps, persistent over items.  The producer streams
+// weight tiles with cp.async.bulk.tensor (128-byte swizzle) and the activation / scale
+// chunks with cp.async into an NSTAGE ring guarded by mbarriers.  Consumer warp w owns tile
+// rows 16w..16w+15: it decodes its weight fragment in registers (cvt e2m1x2 / e4m3x2 ->
+// f16x2), runs m16n8k16 MMAs per 32-wide K block against every 8-row activation tile, and
+// applies the block's E8M0 scale to the block's f32 result.  Within a 32-wide block the
+// MMA's 16 K slots are a fixed permutation of the block's K positions, applied to both
+// operands, which leaves the dot product unchanged.
+#pragma once
+
+#include "common.cuh"
+
+namespace mono {
+
+constexpr int MAX_EXPERTS = 256;
+constexpr int EXPERT_ROWS = 16;  // routed rows per expert work item
+constexpr int TILE_M = 64;       // weight rows per work item
+constexpr int BOX_ROWS = 32;     // rows per TMA box; two boxes per stage
+constexpr int BOX_BYTES = 128;   // bytes per row per box = the 128-byte swizzle span
+constexpr int W_STAGE_BYTES = TILE_M * BOX_BYTES;
+constexpr int CONSUMER_WARPS = 4;
+constexpr int GEMM_THREADS = (CONSUMER_WARPS + 1) * 32;
+
+// Routing metadata written by the top-k kernel and read by the expert GEMMs.
+struct RouteInfo {
+  int n_hit;                       // experts with at least one routed row
+  int hit_e[MAX_EXPERTS];          // expert id of the d-th hit expert (increasing)
+  int hit_off[MAX_EXPERTS];        // first expert-sorted position of its rows
+  int hit_cnt[MAX_EXPERTS];        // number of rows routed to it
+  int rg_prefix[MAX_EXPERTS + 1];  // prefix sum of ceil(hit_cnt / EXPERT_ROWS)
+};
+
+enum : int { EPI_BF16 = 0, EPI_F16 = 1, EPI_RESID_BF16 = 2, EPI_SWIGLU_F16 = 3, EPI_F32 = 4 };
+
+struct GemmParams {
+  const uint8_t* scales;  // E8M0 scales (fmt 8: [N/32, K/32]; fmt 4: [E*N, K/32])
+  long long scale_ld;     // bytes per scale row (K/32)
+  int K;                  // reduction length in elements (multiple of 128)
+  int N;                  // weight rows per matrix
+  int rows_per_mat;       // tensor-map rows per expert matrix (expert mode)
+  int swiglu_I;           // > 0: tile t = gate rows [32t, 32t+32) and up rows I + [32t, 32t+32)
+  const __half* act;      // activations, f16 [*, act_ld]
+  int act_ld;
+  const int* act_rowmap;  // expert mode: sorted position -> activation row (or null)
+  int dense_rows;         // dense mode: activation rows
+  int n_tiles;            // work tiles per matrix
+  int ksplit;             // dense mode: K splits per tile
+  const RouteInfo* route; // non-null selects expert mode
+  int epi;
+  void* out;
+  int out_ld;
+  const __nv_bfloat16* resid;  // EPI_RESID_BF16: added before rounding
+  int resid_ld;
+  float clamp;                 // EPI_SWIGLU_F16
+  float* ws;                   // split-K partial tiles
+  int* counters;               // split-K arrival counters, one per tile, left at zero
+  int* status;
+};
+
+template <int FMT>
+struct FmtTraits;
+template <>
+struct FmtTraits<8> {
+  static constexpr int KC = 128;               // K elements per stage (128 bytes per row)
+  static constexpr int ACT_STRIDE = 128 * 2 + 32;  // bytes per activation row (bank spread)
+  static constexpr int SC_BYTES = 8;           // 2 block rows x 4 K blocks
+};
+template <>
+struct FmtTraits<4> {
+  static constexpr int KC = 256;
+  static constexpr int ACT_STRIDE = 256 * 2 + 64;
+  static constexpr int SC_BYTES = TILE_M * 8;  // 64 weight rows x 8 K blocks
+};
+
+__host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+template <int FMT, int NT, int NSTAGE>
+struct GemmLayout {
+  static constexpr int ROWS = NT * 8;
+  static constexpr int ACT_BYTES = ROWS * FmtTraits<FMT>::ACT_STRIDE;
+  static constexpr int SC_BYTES = FmtTraits<FMT>::SC_BYTES;
+  static constexpr int EP_LD = ROWS + 1;  // odd stride: conflict-free column reads
+  static constexpr int W_OFF = 0;         // 1024-aligned (128-byte swizzle)
+  static constexpr int ACT_OFF = NSTAGE * W_STAGE_BYTES;
+  static constexpr int SC_OFF = ACT_OFF + NSTAGE * ACT_BYTES;
+  static constexpr int EP_OFF = align_up(SC_OFF + NSTAGE * SC_BYTES, 16);
+  static constexpr int BAR_OFF = align_up(EP_OFF + TILE_M * EP_LD * 4, 16);
+  static constexpr int MISC_OFF = BAR_OFF + 2 * NSTAGE * 8;
+  static constexpr int BYTES = MISC_OFF + 16 + 1024;  // + slack for 1024-byte alignment
+};
+
+struct Item {
+  int wrow_a, wrow_b;  // tensor-map rows of the two boxes
+  int sc_a, sc_b;      // scale rows of the two boxes
+  bool a_ok, b_ok;     // boxes start inside the matrix
+  int k0, nck;         // first K element, number of stages
+  int n;               // activation rows
+  int row0;            // first output row (expert mode: sorted position)
+  int tile, split;
+  int col0;            // first output column
+};
+
+template <int FMT>
+__device__ __forceinline__ void decode_item(const GemmParams& p, int q, Item& it) {
+  constexpr int KC = FmtTraits<FMT>::KC;
+  int base = 0;
+  if (p.route) {
+    const RouteInfo& R = *p.route;
+    int lo = 0, hi = R.n_hit - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (R.rg_prefix[mid] * p.n_tiles <= q) lo = mid; else hi = mid - 1;
+    }
+    const int d = lo;
+    const int rgc = R.rg_prefix[d + 1] - R.rg_prefix[d];
+    const int local = q - R.rg_prefix[d] * p.n_tiles;
+    it.tile = local / rgc;
+    const int rg = local - it.tile * rgc;
+    it.split = 0;
+    base = R.hit_e[d] * p.rows_per_mat;
+    it.n = min(EXPERT_ROWS, R.hit_cnt[d] - rg * EXPERT_ROWS);
+    it.row0 = R.hit_off[d] + rg * EXPERT_ROWS;
+    it.k0 = 0;
+    it.nck = (p.K + KC - 1) / KC;
+  } else {
+    it.tile = q / p.ksplit;
+    it.split = q - it.tile * p.ksplit;
+    const int nck_all = (p.K + KC - 1) / KC;
+    const int cps = (nck_all + p.ksplit - 1) / p.ksplit;
+    const int c0 = it.split * cps;
+    it.nck = max(0, min(cps, nck_all - c0));
+    it.k0 = c0 * KC;
+    it.n = p.dense_rows;
+    it.row0 = 0;
+  }
+  int ra, rb;
+  if (p.swiglu_I > 0) {
+    ra = BOX_ROWS * it.tile;
+    rb = p.swiglu_I + BOX_ROWS * it.tile;
+    it.col0 = BOX_ROWS * it.tile;
+  } else {
+    ra = TILE_M * it.tile;
+    rb = ra + BOX_ROWS;
+    it.col0 = ra;
+  }
+  it.a_ok = ra < p.N;
+  it.b_ok = rb < p.N;
+  it.wrow_a = base + ra;
+  it.wrow_b = base + rb;
+  if (FMT == 8) {
+    it.sc_a = ra / 32;
+    it.sc_b = rb / 32;
+  } else {
+    it.sc_a = base + ra;
+    it.sc_b = base + rb;
+  }
+}
+
+__device__ __forceinline__ int total_items(const GemmParams& p) {
+  return p.route ? p.route->rg_prefix[p.route->n_hit] * p.n_tiles : p.n_tiles * p.ksplit;
+}
+
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(CONSUMER_WARPS * 32)); }
+
+// Waits on an mbarrier phase; gives up when another warp of the CTA has aborted or the
+// time budget runs out (then raises the status bit and the CTA's abort flag).
+__device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > WAIT_BUDGET_NS) {
+      atomicOr(status, ST_WAIT_TIMEOUT);
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------------------ producer
+template <int FMT, int NT, int NSTAGE>
+__device__ void gemm_producer(const GemmParams& p, const CUtensorMap* map, uint8_t* smem,
+                              uint64_t* full, uint64_t* empty, volatile int* abort) {
+  using L = GemmLayout<FMT, NT, NSTAGE>;
+  constexpr int KC = FmtTraits<FMT>::KC;
+  constexpr int ASTR = FmtTraits<FMT>::ACT_STRIDE;
+  constexpr int CPR = KC * 2 / 16;  // 16-byte chunks per activation row per stage
+  const int lane = threadIdx.x & 31;
+  const int n_items = total_items(p);
+  int iter = 0;
+  for (int q = blockIdx.x; q < n_items; q += gridDim.x) {
+    Item it;
+    decode_item<FMT>(p, q, it);
+    for (int c = 0; c < it.nck; ++c, ++iter) {
+      const int s = iter % NSTAGE;
+      const uint32_t ph = (iter / NSTAGE) & 1;
+      if (!pipe_wait(&empty[s], ph ^ 1, p.status, abort)) goto drain;
+      {
+        const int k0 = it.k0 + c * KC;
+        const int kvalid = min(KC, p.K - k0);
+        // activations: rows 0..n-1 of this item, zero-filled past K
+        uint8_t* ast = smem + L::ACT_OFF + s * L::ACT_BYTES;
+        const int vbytes = kvalid * 2;
+        for (int idx = lane; idx < it.n * CPR; idx += 32) {
+          const int i = idx / CPR, ch = idx - i * CPR;
+          int arow = i;
+          if (p.route) arow = p.act_rowmap ? p.act_rowmap[it.row0 + i] : it.row0 + i;
+          const bool ok = ch * 16 < vbytes;
+          const __half* src = p.act + (long long)arow * p.act_ld + k0 + ch * 8;
+          cp_async16(ast + i * ASTR + ch * 16, ok ? (const void*)src : (const void*)p.act,
+                     ok ? 16u : 0u);
+        }
+        // scales of the stage's K blocks
+        uint8_t* sst = smem + L::SC_OFF + s * L::SC_BYTES;
+        const int kb0 = k0 / 32, nkb = kvalid / 32;
+        if (FMT == 8) {
+          if (lane < 2) {
+            const bool ok = lane == 0 ? it.a_ok : it.b_ok;
+            const int row = lane == 0 ? it.sc_a : it.sc_b;
+            const uint8_t* src = p.scales + row * p.scale_ld + kb0;
+            cp_async4(sst + lane * 4, ok ? (const void*)src : (const void*)p.scales,
+                      ok ? (uint32_t)min(4, nkb) : 0u);
+          }
+        } else {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const bool ok = half == 0 ? it.a_ok : it.b_ok;
+            const long long row = (long long)(half == 0 ? it.sc_a : it.sc_b) + lane;
+            const uint8_t* src = p.scales + row * p.scale_ld + kb0;
+            uint8_t* dst = sst + (half * BOX_ROWS + lane) * 8;
+            const int n0 = ok ? min(4, nkb) : 0, n1 = ok ? max(0, min(4, nkb - 4)) : 0;
+            cp_async4(dst, n0 ? (const void*)src : (const void*)p.scales, (uint32_t)n0);
+            cp_async4(dst + 4, n1 ? (const void*)(src + 4) : (const void*)p.scales, (uint32_t)n1);
+          }
+        }
+        cp_async_arrive_noinc(&full[s]);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], W_STAGE_BYTES);
+          const int xb = FMT == 8 ? k0 : k0 / 2;
+          uint8_t* wst = smem + L::W_OFF + s * W_STAGE_BYTES;
+          tma_load_2d(wst, map, xb, it.wrow_a, &full[s]);
+          tma_load_2d(wst + BOX_ROWS * BOX_BYTES, map, xb, it.wrow_b, &full[s]);
+        }
+      }
+    }
+  }
+  return;
+drain:
+  // A wait failed: let the copies already issued land before the CTA exits.
+  for (int k = 1; k <= NSTAGE && k <= iter; ++k) {
+    const int j = iter - k;
+    mbar_wait(&full[j % NSTAGE], (j / NSTAGE) & 1, p.status, 100000000ull);
+  }
+}
+
+// ------------------------------------------------------------------------------ epilogue
+__device__ __forceinline__ float swiglu_clamped(float g, float u, float c) {
+  g = fminf(fmaxf(g, -c), c);
+  u = fminf(fmaxf(u, -c), c);
+  return g / (1.0f + expf(-g)) * u;
+}
+
+template <int EP_LD, int ROWS>
+__device__ void gemm_epilogue(const GemmParams& p, const Item& it, float* ep, int tid,
+                              volatile int* flag) {
+  const int n = it.n;
+  if (p.route == nullptr && p.ksplit > 1) {
+    // fixed-order split-K reduction: every split stores its tile, the last one sums them
+    float* ws_tile = p.ws + (size_t)it.tile * p.ksplit * TILE_M * ROWS;
+    float* mine = ws_tile + (size_t)it.split * TILE_M * ROWS;
+    for (int idx = tid; idx < TILE_M * n; idx += CONSUMER_WARPS * 32) {
+      const int i = idx / TILE_M, m = idx - i * TILE_M;
+      mine[m * ROWS + i] = ep[m * EP_LD + i];
+    }
+    __threadfence();
+    consumer_bar();
+    if (tid == 0) *flag = (atomicAdd(&p.counters[it.tile], 1) == p.ksplit - 1);
+    consumer_bar();
+    if (!*flag) return;
+    __threadfence();
+    for (int idx = tid; idx < TILE_M * n; idx += CONSUMER_WARPS * 32) {
+      const int i = idx / TILE_M, m = idx - i * TILE_M;
+      float v = 0.0f;
+      for (int s = 0; s < p.ksplit; ++s) v += __ldcg(ws_tile + ((size_t)s * TILE_M + m) * ROWS + i);
+      ep[m * EP_LD + i] = v;
+    }
+    consumer_bar();
+    if (tid == 0) p.counters[it.tile] = 0;
+  }
+  if (p.epi == EPI_SWIGLU_F16) {
+    __half* out = reinterpret_cast<__half*>(p.out);
+    for (int idx = tid; idx < BOX_ROWS * n; idx += CONSUMER_WARPS * 32) {
+      const int i = idx / BOX_ROWS, m = idx - i * BOX_ROWS;
+      const int col = it.col0 + m;
+      if (col >= p.swiglu_I) continue;
+      const float t = swiglu_clamped(ep[m * EP_LD + i], ep[(m + BOX_ROWS) * EP_LD + i], p.clamp);
+      out[(size_t)(it.row0 + i) * p.out_ld + col] = bf16_as_f16(t);
+    }
+    return;
+  }
+  for (int idx = tid; idx < TILE_M * n; idx += CONSUMER_WARPS * 32) {
+    const int i = idx / TILE_M, m = idx - i * TILE_M;
+    const int col = it.col0 + m;
+    if (col >= p.N) continue;
+    const float v = ep[m * EP_LD + i];
+    const size_t o = (size_t)(it.row0 + i) * p.out_ld + col;
+    switch (p.epi) {
+      case EPI_BF16:
+        reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(v);
+        break;
+      case EPI_F16:
+        reinterpret_cast<__half*>(p.out)[o] = bf16_as_f16(v);
+        break;
+      case EPI_RESID_BF16: {
+        const float r = __bfloat162float(p.resid[(size_t)(it.row0 + i) * p.resid_ld + col]);
+        reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(r + v);
+        break;
+      }
+      default:
+        reinterpret_cast<float*>(p.out)[o] = v;
+        break;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------ consumer
+template <int FMT, int NT, int NSTAGE>
+__device__ void gemm_consumer(const GemmParams& p, uint8_t* smem, uint64_t* full,
+                              uint64_t* empty, volatile int* abort, volatile int* flag) {
+  using L = GemmLayout<FMT, NT, NSTAGE>;
+  constexpr int ASTR = FmtTraits<FMT>::ACT_STRIDE;
+  const int tid = threadIdx.x;  // 0..127
+  const int w = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int r0 = 16 * (w & 1) + g;  // row of this thread inside its 32-row box
+  float* ep = reinterpret_cast<float*>(smem + L::EP_OFF);
+  const int n_items = total_items(p);
+  int iter = 0;
+  for (int q = blockIdx.x; q < n_items; q += gridDim.x) {
+    Item it;
+    decode_item<FMT>(p, q, it);
+    const int ntl = (it.n + 7) >> 3;
+    float acc[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.0f;
+
+    for (int ck = 0; ck < it.nck; ++ck, ++iter) {
+      const int s = iter % NSTAGE;
+      if (!pipe_wait(&full[s], (iter / NSTAGE) & 1, p.status, abort)) return;
+      const uint8_t* wbox = smem + L::W_OFF + s * W_STAGE_BYTES + (w >> 1) * (BOX_ROWS * BOX_BYTES);
+      const uint8_t* wr0 = wbox + r0 * BOX_BYTES;
+      const uint8_t* wr1 = wr0 + 8 * BOX_BYTES;
+      const uint8_t* sc = smem + L::SC_OFF + s * L::SC_BYTES;
+      const uint8_t* act = smem + L::ACT_OFF + s * L::ACT_BYTES + g * ASTR;
+      if (FMT == 4) {
+        const uint2 sa8 = lds64(sc + (16 * w + g) * 8);
+        const uint2 sb8 = lds64(sc + (16 * w + g + 8) * 8);
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          const int off = ((b ^ g) << 4) + (c << 2);
+          uint32_t ha[4], hb[4];
+          e2m1x8_to_f16x8(lds32(wr0 + off), ha);
+          e2m1x8_to_f16x8(lds32(wr1 + off), hb);
+          const uint32_t A0[4] = {ha[0], hb[0], ha[1], hb[1]};
+          const uint32_t A1[4] = {ha[2], hb[2], ha[3], hb[3]};
+          const uint32_t sa_b = ((b < 4 ? sa8.x : sa8.y) >> (8 * (b & 3))) & 0xFFu;
+          const uint32_t sb_b = ((b < 4 ? sb8.x : sb8.y) >> (8 * (b & 3))) & 0xFFu;
+          const float sa = e8m0_to_f32(sa_b), sb = e8m0_to_f32(sb_b);
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            if (t < ntl) {
+              const uint4 bv = lds128(act + t * 8 * ASTR + (32 * b + 8 * c) * 2);
+              float d[4];
+              mma_f16(d, A0, bv.x, bv.y);
+              mma_f16_acc(d, A1, bv.z, bv.w);
+              acc[t][0] = fmaf(sa, d[0], acc[t][0]);
+              acc[t][1] = fmaf(sa, d[1], acc[t][1]);
+              acc[t][2] = fmaf(sb, d[2], acc[t][2]);
+              acc[t][3] = fmaf(sb, d[3], acc[t][3]);
+            }
+          }
+        }
+      } else {
+        const uint32_t sc4 = lds32(sc + (w >> 1) * 4);
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int off0 = (((2 * b) ^ g) << 4) + (c << 2);
+          const int off1 = (((2 * b + 1) ^ g) << 4) + (c << 2);
+          uint32_t ha0[2], hb0[2], ha1[2], hb1[2];
+          e4m3x4_to_f16x4(lds32(wr0 + off0), ha0);
+          e4m3x4_to_f16x4(lds32(wr1 + off0), hb0);
+          e4m3x4_to_f16x4(lds32(wr0 + off1), ha1);
+          e4m3x4_to_f16x4(lds32(wr1 + off1), hb1);
+          const uint32_t A0[4] = {ha0[0], hb0[0], ha0[1], hb0[1]};
+          const uint32_t A1[4] = {ha1[0], hb1[0], ha1[1], hb1[1]};
+          const float sf = e8m0_to_f32((sc4 >> (8 * b)) & 0xFFu);
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            if (t < ntl) {
+              const uint2 b0 = lds64(act + t * 8 * ASTR + (32 * b + 4 * c) * 2);
+              const uint2 b1 = lds64(act + t * 8 * ASTR + (32 * b + 16 + 4 * c) * 2);
+              float d[4];
+              mma_f16(d, A0, b0.x, b0.y);
+              mma_f16_acc(d, A1, b1.x, b1.y);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) acc[t][j] = fmaf(sf, d[j], acc[t][j]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+    // tile result -> shared memory, then the fused epilogue
+    const int m0 = 16 * w + g;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      if (t < ntl) {
+        const int col = t * 8 + 2 * c;
+        ep[m0 * L::EP_LD + col] = acc[t][0];
+        ep[m0 * L::EP_LD + col + 1] = acc[t][1];
+        ep[(m0 + 8) * L::EP_LD + col] = acc[t][2];
+        ep[(m0 + 8) * L::EP_LD + col + 1] = acc[t][3];
+      }
+    }
+    if (*abort) return;
+    consumer_bar();
+    gemm_epilogue<L::EP_LD, L::ROWS>(p, it, ep, tid, flag);
+    consumer_bar();
+  }
+}
+
+template <int FMT, int NT, int NSTAGE>
+__global__ void __launch_bounds__(GEMM_THREADS)
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap map, const GemmParams p) {
+  using L = GemmLayout<FMT, NT, NSTAGE>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
+  uint64_t* empty = full + NSTAGE;
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::MISC_OFF);
+  volatile int* flag = abort + 1;
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full[s], 1 + 32);  // expect_tx arrival + one cp.async arrival per lane
+      mbar_init(&empty[s], CONSUMER_WARPS);
+    }
+    fence_mbar_init();
+    *abort = 0;
+  }
+  if (warp == CONSUMER_WARPS && (threadIdx.x & 31) == 0) prefetch_tmap(&map);
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();
+  if (warp == CONSUMER_WARPS)
+    gemm_producer<FMT, NT, NSTAGE>(p, &map, smem, full, empty, abort);
+  else
+    gemm_consumer<FMT, NT, NSTAGE>(p, smem, full, empty, abort, flag);
+}
+
+}  // namespace mono

@@ -150,6 +150,14 @@ def bf16_bits(v: float) -> int:
     return int(lib().orc_bf16_bits(v))
 
 
+def bf16_round_array(v) -> np.ndarray:
+    """float64 array -> bf16 bit patterns, round to nearest even (orc_bf16_bits per element)."""
+    v = _c(v, np.float64)
+    out = np.empty(v.shape, np.uint16)
+    lib().orc_bf16_bits_array(_p(v), C.c_size_t(v.size), _p(out))
+    return out
+
+
 def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     """uint16 bf16 bit patterns -> float64 values."""
     b = np.asarray(bits, dtype=np.uint16)
@@ -308,6 +316,6 @@ def layer(spec: dict, weights: dict, step: dict, force_idx=None):
 
 
 __all__ = ["build", "lib", "set_threads", "get_threads", "e8m0", "e4m3", "e2m1", "encode_e4m3",
-           "round_bf16", "bf16_bits", "bf16_to_f64", "swiglu", "rmsnorm", "gemv_mxfp8",
+           "round_bf16", "bf16_bits", "bf16_round_array", "bf16_to_f64", "swiglu", "rmsnorm", "gemv_mxfp8",
            "gemv_mxfp4", "kv_quant", "attend", "router", "ffn", "key_range", "kv_insert",
            "attention", "layer"]

@@ -109,6 +109,10 @@ uint16_t orc_bf16_bits(double v) {
   return (uint16_t)(u >> 16);
 }
 
+void orc_bf16_bits_array(const double *v, size_t n, uint16_t *out) {
+  for (size_t i = 0; i < n; i++) out[i] = orc_bf16_bits(v[i]);
+}
+
 double orc_bf16_value(uint16_t b) {
   uint32_t u = (uint32_t)b << 16;
   float f;

@@ -19,6 +19,7 @@
  */
 #ifndef MONO_ORACLE_H
 #define MONO_ORACLE_H
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -74,6 +75,7 @@ double orc_e2m1(uint8_t nibble);
 uint8_t orc_encode_e4m3(float v);
 double orc_round_bf16(double v);
 uint16_t orc_bf16_bits(double v);
+void orc_bf16_bits_array(const double *v, size_t n, uint16_t *out);
 double orc_bf16_value(uint16_t bits);
 
 /* stages */
