@@ -1,0 +1,488 @@
+"""Benchmark of the fused MoE decode layer on GB300: microseconds per layer step and the HBM
+bandwidth it sustains, on synthetic seeded inputs.
+
+Headline workload: one full-size layer at 48 rows (8 requests x 6 rows, causal window 128,
+contexts uniform in [1024, 65536], 128 experts top-6), the configuration the 60%-of-HBM
+target is set on.  The same JSON line carries the 1-row and 6-row (draft, top-3,
+non-causal 192-wide rows) shapes under "rows_sweep".
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+* value: device time per layer step, K steps replayed from CUDA graphs with every input
+  resident in HBM; the layer's weights rotate over several distinct copies so that no step
+  finds its weights in L2.
+* e2e: the same step through the public C ABI from pinned host buffers (inputs copied in,
+  output copied out, every step).
+* roofline: the dominant kernel's algorithmic bytes per launch over its CUDA-event time.
+* cpu_baseline: the CPU oracle on the host cores (a reported baseline only).
+* --impl reference: the oracle, timed as it stands, is the reference arm.
+Under torchrun each rank runs an independent replica (no collective in the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gen  # noqa: E402
+
+METRIC = "us per fused decode-layer step (achieved HBM GB/s vs ~8 TB/s at rows 1/6/48)"
+UNIT = "us/step"
+HEADLINE = "full_r48"
+NOMINAL_HBM_GBS = 8000.0
+KV_BYTES_READ = 516  # per cached token read: 512 e4m3 codes + f32 scale (pad not counted)
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------------------- bytes
+def step_bytes(spec: dict, step: dict, topk_idx: np.ndarray) -> dict:
+    """Algorithmic bytes of one step: every weight, scale and KV record it must touch, once.
+
+    attention + shared + router + norm weights, the hit experts (D_hit x one expert's
+    MXFP4 gate_up + down incl. scales), the union of each request's windows of KV records,
+    the KV records written, and the hidden rows read and written."""
+    wb = gen.weight_bytes(spec)
+    valid = np.asarray(step["positions"].cpu()) >= 0
+    d_hit = len(np.unique(topk_idx[valid]))
+    pos = np.asarray(step["positions"].cpu())
+    req = np.asarray(step["row_req"].cpu())
+    kv_tokens = 0
+    for q in np.unique(req[valid]):
+        ps = pos[(req == q) & valid]
+        keys = set()
+        for p in ps:
+            hi = p if spec["causal"] else ps.max()
+            width = spec["window"] if spec["causal"] else spec["swa_width"]
+            keys.update(range(max(0, hi - width + 1), hi + 1))
+        kv_tokens += len(keys)
+    rows = int(valid.sum())
+    H = spec["hidden"]
+    kv_rec = spec["kv_dim"] + 4
+    b = dict(attn=wb["attn"], shared=wb["shared"], router=wb["router"], norms=wb["norms"],
+             experts=d_hit * wb["expert"], kv_read=kv_tokens * kv_rec, kv_write=rows * kv_rec,
+             hidden=2 * rows * H * 2)
+    b["total"] = sum(b.values())
+    b["d_hit"] = d_hit
+    return b
+
+
+def expert_gate_up_bytes(spec, d_hit, n_slots, rows):
+    """Per-launch algorithmic bytes of the routed gate_up GEMM: the hit experts' MXFP4
+    gate_up weights and scales, the normed rows it reads, the SwiGLU rows it writes."""
+    H, I = spec["hidden"], spec["moe_inter"]
+    w = 2 * I * H // 2 + 2 * I * (H // 32)
+    return d_hit * w + rows * H * 2 + n_slots * I * 2
+
+
+def expert_down_bytes(spec, d_hit, n_slots):
+    H, I = spec["hidden"], spec["moe_inter"]
+    w = H * I // 2 + H * (I // 32)
+    return d_hit * w + n_slots * I * 2 + n_slots * H * 4
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (SM clock, max clock, throttle reasons) while the GPU works."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.p:
+            time.sleep(0.1)
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+        self.f.flush()
+
+    def summary(self):
+        self.f.seek(0)
+        rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                clk, mxc = float(r[1]), float(r[2])
+            except (ValueError, IndexError):
+                continue
+            mx = mxc
+            sm.append(clk)
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        load = [c for c in sm if c > 0.5 * (mx or max(sm))] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ our arm
+def _layer_copies(name, n_copies, dev, seed0=None):
+    import moe_decode_layer_mxfp8_gb300 as m
+    wl = gen.WORKLOADS[name]
+    spec = gen.spec_of(name)
+    step = gen.make_step(spec, wl, device=dev)
+    spec["max_rows"] = step["rows"]
+    layers = []
+    base = wl["seed"] if seed0 is None else seed0
+    for c in range(n_copies):
+        w = gen.make_weights(spec, base + 1000 * c, device=dev)
+        layers.append((m.Layer(spec, w), w))
+    return spec, step, layers
+
+
+def _capture(layers, step, outs, stream, n_steps):
+    """A graph of n_steps layer steps rotating over the copies."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(n_steps):
+            lay, _ = layers[i % len(layers)]
+            lay.step(step["x"], outs[i % len(layers)], step["positions"], step["row_req"],
+                     step["block_table"], step["kv_cache"], stream=stream)
+    return g
+
+
+def measure_device(name, steps, warmup, dev, n_copies, sampler=None):
+    spec, step, layers = _layer_copies(name, n_copies, dev)
+    C = len(layers)
+    outs = [torch.empty_like(step["x"]) for _ in range(C)]
+    stream = torch.cuda.Stream(dev)
+    idx = torch.empty((step["rows"], spec["topk"]), dtype=torch.int32, device=dev)
+    # routing of every copy (for the bytes it touches), eager
+    byte_list = []
+    with torch.cuda.stream(stream):
+        for c, (lay, _) in enumerate(layers):
+            lay.step(step["x"], outs[c], step["positions"], step["row_req"], step["block_table"],
+                     step["kv_cache"], stream=stream, topk_idx_out=idx)
+            stream.synchronize()
+            byte_list.append(step_bytes(spec, step, idx.cpu().numpy()))
+        for lay, _ in layers:
+            assert lay.status() == 0
+        big_n = C * max(1, 64 // C)
+        big = _capture(layers, step, outs, stream, big_n)
+        ones = [_capture([layers[c]], step, [outs[c]], stream, 1) for c in range(C)]
+    torch.cuda.synchronize(dev)
+
+    def run(k):
+        for _ in range(k // big_n):
+            big.replay()
+        for i in range(k % big_n):
+            ones[i % C].replay()
+
+    with torch.cuda.stream(stream):
+        run(max(warmup, 3))
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if torch.distributed.is_initialized():
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        run(steps)
+        t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1)
+    if torch.distributed.is_initialized():
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+    us = ms * 1000.0 / steps
+    # bytes per step averaged over the rotation actually run
+    seq = [byte_list[i % C]["total"] for i in range(steps)]
+    avg_bytes = float(np.mean(seq))
+    res = dict(spec=spec, step=step, layers=layers, outs=outs, stream=stream, us=us, ms=ms,
+               bytes=avg_bytes, bytes_detail=byte_list[0], d_hit=[b["d_hit"] for b in byte_list],
+               launches=steps * layers[0][0].launches_per_step(), copies=C)
+    return res
+
+
+def kernel_profile(res, dev, reps=20):
+    """Per-launch CUDA-event times (eager steps, programmatic overlap off while profiling)."""
+    spec, step, layers, stream = res["spec"], res["step"], res["layers"], res["stream"]
+    lay0 = layers[0][0]
+    n = lay0.launches_per_step()
+    names = lay0.launch_names()
+    per = {k: [] for k in names}
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    with torch.cuda.stream(stream):
+        for e in evs:
+            e.record(stream)
+        for lay, _ in layers:
+            lay.set_profile_events(evs)
+        for i in range(reps + 3):
+            lay, _ = layers[i % len(layers)]
+            lay.step(step["x"], res["outs"][i % len(layers)], step["positions"], step["row_req"],
+                     step["block_table"], step["kv_cache"], stream=stream)
+            stream.synchronize()
+            if i >= 3:
+                for j, k in enumerate(names):
+                    per[k].append(evs[j].elapsed_time(evs[j + 1]) * 1000.0)
+        for lay, _ in layers:
+            lay.set_profile_events(None)
+    torch.cuda.synchronize(dev)
+    return {k: float(np.mean(v)) for k, v in per.items()}
+
+
+def measure_e2e(res, steps, warmup, dev):
+    """Public API with host buffers: pinned inputs copied in and the output copied out
+    every step, all inside the timed region."""
+    spec, step, layers = res["spec"], res["step"], res["layers"]
+    stream = res["stream"]
+    rows, H = step["rows"], spec["hidden"]
+    h_x = step["x"].cpu().pin_memory()
+    h_pos = step["positions"].cpu().pin_memory()
+    h_req = step["row_req"].cpu().pin_memory()
+    h_tab = step["block_table"].cpu().pin_memory()
+    h_out = torch.empty((rows, H), dtype=torch.bfloat16).pin_memory()
+    d_x = torch.empty_like(step["x"])
+    d_pos, d_req, d_tab = (torch.empty_like(step[k]) for k in ("positions", "row_req", "block_table"))
+    d_out = torch.empty_like(step["x"])
+
+    def one(i):
+        lay, _ = layers[i % len(layers)]
+        d_x.copy_(h_x, non_blocking=True)
+        d_pos.copy_(h_pos, non_blocking=True)
+        d_req.copy_(h_req, non_blocking=True)
+        d_tab.copy_(h_tab, non_blocking=True)
+        lay.step(d_x, d_out, d_pos, d_req, d_tab, step["kv_cache"], stream=stream)
+        h_out.copy_(d_out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, warmup)):
+            one(i)
+        stream.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(steps):
+            one(i)
+        t1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = t0.elapsed_time(t1) * 1000.0 / steps
+    h2d = sum(t.numel() * t.element_size() for t in (h_x, h_pos, h_req, h_tab))
+    d2h = h_out.numel() * h_out.element_size()
+    return dict(value=us, unit=UNIT, h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h))
+
+
+def cpu_baseline(res):
+    """The oracle, as it stands, on the host cores: one full layer step of the headline
+    workload (all rows) on every core."""
+    import oracle
+    from tests.helpers import to_np
+    spec, step = res["spec"], res["step"]
+    w = {k: to_np(v) for k, v in res["layers"][0][1].items()}
+    s = {k: (to_np(v) if isinstance(v, torch.Tensor) else v) for k, v in step.items()}
+    cores = os.cpu_count() or 1
+    oracle.set_threads(cores)
+    t = time.perf_counter()
+    oracle.layer(spec, w, s)
+    dt = time.perf_counter() - t
+    return dict(value=dt * 1e6, unit=UNIT, cores=cores, kind="oracle",
+                sample=f"one full {res['step']['rows']}-row layer step of the headline workload "
+                       f"(weights copy 0), OpenMP over {cores} host threads")
+
+
+# ------------------------------------------------------------------------ reference arm
+def run_reference(args, rank):
+    """The oracle as the reference arm: K timed steps of the headline workload on the host
+    cores (each step a full layer step; rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    from tests.helpers import np_inputs
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    spec = gen.spec_of(HEADLINE)
+    wl = gen.WORKLOADS[HEADLINE]
+    w = gen.make_weights(spec, wl["seed"], device=dev)
+    st = gen.make_step(spec, wl)
+    wn, sn = np_inputs(w, st)
+    cores = os.cpu_count() or 1
+    oracle.build()
+    oracle.set_threads(cores)
+    for _ in range(args.warmup):
+        oracle.layer(spec, wn, sn)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.layer(spec, wn, sn)
+    dt = (time.perf_counter() - t) / args.steps
+    v = dt * 1e6
+    line = dict(impl="reference", metric=METRIC, value=v, unit=UNIT, n_gpus=args.gpus,
+                steps=args.steps, warmup=args.warmup, ms_per_step=dt * 1e3,
+                higher_is_better=False, scaling="weak", vs_baseline=None, dtype="f64",
+                data="synthetic",
+                config=dict(workload=_workload_desc(HEADLINE, spec, st["rows"]),
+                            l2="n/a (host)"),
+                cpu_baseline=dict(value=v, unit=UNIT, cores=cores, kind="oracle",
+                                  sample=f"each step one full {st['rows']}-row layer step, "
+                                         f"OpenMP over {cores} host threads"),
+                e2e=dict(value=v, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0),
+                gpu_launches=0)
+    print(json.dumps(line), flush=True)
+
+
+def _workload_desc(name, spec, rows):
+    d = {"full_r48": "MoE decode layer, full size, 48 rows (8 requests x 6), causal window 128, "
+                     "contexts U[1024,65536], 128 experts top-6",
+         "full_r1": "MoE decode layer, full size, 1 row, causal window 128, context 8192, top-6",
+         "draft_r6": "MoE decode layer, full size, 6 draft rows, non-causal 192-wide, "
+                     "context 65536, top-3"}[name]
+    return (f"{d}; hidden {spec['hidden']}, {spec['n_q_heads']}x{spec['head_dim']} q heads, "
+            f"kv latent {spec['kv_dim']}, MXFP8 attention/shared, MXFP4 experts "
+            f"(moe {spec['moe_inter']}, shared {spec['shared_inter']})")
+
+
+# ------------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-sweep", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--workload", default=HEADLINE, choices=["full_r48", "full_r1", "draft_r6"])
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    if args.impl == "reference":
+        run_reference(args, rank)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    from moe_decode_layer_mxfp8_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    peak, peak_kind = _peaks()
+
+    def copies_for(name):
+        """Distinct layer copies so that the weights one rotation touches exceed 3x L2."""
+        spec, wl = gen.spec_of(name), gen.WORKLOADS[name]
+        wb = gen.weight_bytes(spec)
+        rpr = wl["rows_per_req"]
+        n_req = int(str(wl["contexts"]).split(":")[-1]) if isinstance(wl["contexts"], str) else len(wl["contexts"])
+        rows = rpr * n_req if isinstance(rpr, int) else sum(rpr)
+        d_hit = min(spec["n_experts"], (1 if wl.get("repeat_input") else rows) * spec["topk"])
+        touched = wb["attn"] + wb["shared"] + wb["router"] + d_hit * wb["expert"]
+        return max(2, int(np.ceil(3 * l2 / touched)))
+
+    with ClockSampler(local) as clk:
+        res = measure_device(args.workload, args.steps, args.warmup, dev, copies_for(args.workload))
+        sweep = {}
+        if not args.no_sweep:
+            for name in ("full_r1", "draft_r6"):
+                if name == args.workload:
+                    continue
+                r = measure_device(name, min(args.steps, 2000), args.warmup, dev, copies_for(name))
+                sweep[name] = dict(rows=r["step"]["rows"], us_per_step=round(r["us"], 2),
+                                   hbm_gbs=round(r["bytes"] / r["us"] / 1e3, 1),
+                                   frac_of_8tbs=round(r["bytes"] / r["us"] / 1e3 / NOMINAL_HBM_GBS, 4),
+                                   bytes_per_step=int(r["bytes"]), d_hit=r["d_hit"])
+                del r
+                torch.cuda.empty_cache()
+    clocks = clk.summary()
+
+    prof = kernel_profile(res, dev)
+    e2e = measure_e2e(res, args.steps if args.steps <= 500 else 500, args.warmup, dev)
+    spec, step = res["spec"], res["step"]
+    rows = step["rows"]
+    # dominant kernel and its roofline
+    top = max(prof, key=prof.get)
+    d_hit = res["bytes_detail"]["d_hit"]
+    n_slots = rows * spec["topk"]
+    if top == "expert_gate_up":
+        alg = expert_gate_up_bytes(spec, d_hit, n_slots, rows)
+    elif top == "expert_down":
+        alg = expert_down_bytes(spec, d_hit, n_slots)
+    else:
+        alg = None
+    roof = None
+    if alg is not None:
+        ach = alg / (prof[top] * 1e-6) / 1e9
+        roof = dict(kernel=top, bound="hbm", achieved=round(ach, 1), peak=peak,
+                    peak_kind=peak_kind, unit="GB/s", frac=round(ach / peak, 4),
+                    traffic=None, bytes_per_launch=int(alg), us_per_launch=round(prof[top], 2))
+    total_prof = sum(prof.values())
+    gbs = res["bytes"] / res["us"] / 1e3
+    line = dict(
+        metric=METRIC, value=round(res["us"], 3), unit=UNIT, n_gpus=world, steps=args.steps,
+        warmup=args.warmup, ms_per_step=round(res["us"] / 1e3, 6), higher_is_better=False,
+        scaling="weak", vs_baseline=None,
+        dtype="f16 x f16 -> f32 tensor-core products of exactly decoded MXFP8/MXFP4 weights and bf16 activations",
+        data="synthetic",
+        config=dict(workload=_workload_desc(args.workload, spec, rows), rows=rows,
+                    layer_copies=res["copies"],
+                    l2=f"inputs larger than L2: weights rotate over {res['copies']} distinct layer "
+                       f"copies ({res['bytes'] / 1e6:.0f} MB touched per step, L2 {l2 / 1e6:.0f} MB)",
+                    graph="CUDA graphs of programmatically serialised launches"),
+        hbm_gbs=round(gbs, 1), frac_of_8tbs=round(gbs / NOMINAL_HBM_GBS, 4),
+        frac_of_measured_copy=round(gbs / peak, 4), bytes_per_step=int(res["bytes"]),
+        d_hit=res["d_hit"],
+        roofline=roof,
+        per_kernel_us={k: round(v, 2) for k, v in prof.items()},
+        per_kernel_share={k: round(v / total_prof, 4) for k, v in prof.items()},
+        rows_sweep=sweep,
+        e2e={k: (round(v, 3) if isinstance(v, float) else v) for k, v in e2e.items()},
+        clocks=clocks,
+        gpu_launches=res["launches"],
+    )
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(res)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -189,6 +189,16 @@ int mono_layer_read_buffer(mono_layer_t *h, int which, void *host_dst, size_t by
 /* Number of kernel launches one mono_layer_step enqueues. */
 int mono_layer_launches_per_step(mono_layer_t *h);
 
+/* Short name of the i-th launch of a step ("attn_norm", "wqkv", ...), or NULL. */
+const char *mono_layer_launch_name(int i);
+
+/* Profiling support.  With `events` non-NULL (an array of launches_per_step + 1
+ * cudaEvent_t), every later mono_layer_step records events[i] just before its i-th launch
+ * and events[launches_per_step] after the last one, and launches without programmatic
+ * overlap, so that consecutive events bracket exactly one kernel.  The array is borrowed
+ * until profiling is turned off again with events = NULL. */
+int mono_layer_set_profile_events(mono_layer_t *h, void *const *events, int n_events);
+
 #ifdef __cplusplus
 }
 #endif

@@ -52,7 +52,8 @@ class StepArgs(C.Structure):
 
 EXPORTS = ["mono_layer_build", "mono_layer_step", "mono_layer_status", "mono_layer_free",
            "mono_layer_strerror", "mono_layer_buffer", "mono_layer_read_buffer",
-           "mono_layer_launches_per_step"]
+           "mono_layer_launches_per_step", "mono_layer_launch_name",
+           "mono_layer_set_profile_events"]
 
 _lib = None
 
@@ -82,6 +83,9 @@ def lib() -> C.CDLL:
                                         C.POINTER(C.c_size_t)]
         L.mono_layer_read_buffer.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_size_t]
         L.mono_layer_launches_per_step.argtypes = [C.c_void_p]
+        L.mono_layer_launch_name.argtypes = [C.c_int]
+        L.mono_layer_launch_name.restype = C.c_char_p
+        L.mono_layer_set_profile_events.argtypes = [C.c_void_p, C.c_void_p, C.c_int]
         _lib = L
     return _lib
 
@@ -171,6 +175,21 @@ class Layer:
 
     def launches_per_step(self) -> int:
         return lib().mono_layer_launches_per_step(self._h)
+
+    def launch_names(self) -> list[str]:
+        return [lib().mono_layer_launch_name(i).decode() for i in range(self.launches_per_step())]
+
+    def set_profile_events(self, events) -> None:
+        """events: list of launches_per_step()+1 torch.cuda.Event (created and recorded once
+        so that they exist), or None to stop profiling."""
+        if events is None:
+            rc = lib().mono_layer_set_profile_events(self._h, None, 0)
+        else:
+            arr = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
+            self._prof = arr
+            rc = lib().mono_layer_set_profile_events(self._h, arr, len(events))
+        if rc != MONO_OK:
+            raise MonoError(rc, "mono_layer_set_profile_events")
 
     def close(self) -> None:
         if self._h:

@@ -23,6 +23,10 @@ using namespace mono;
 namespace {
 
 constexpr int kLaunchesPerStep = 15;
+const char* const kLaunchNames[kLaunchesPerStep] = {
+    "attn_norm", "wqkv", "qkv_norm_insert", "wq_b", "attention", "wo_a", "wo_b", "ffn_norm",
+    "router", "topk_group", "shared_gate_up", "shared_down", "expert_gate_up", "expert_down",
+    "final"};
 
 enum DenseId { D_WQKV = 0, D_WQB, D_WOA, D_WOB, D_SHGU, D_SHD, D_COUNT };
 
@@ -55,6 +59,8 @@ struct mono_layer {
   int ctas_gemm8[7] = {};  // by nt
   int ctas_gemm4 = 0;
   int attn_min_splits = 1;
+  cudaEvent_t prof[kLaunchesPerStep + 1] = {};
+  bool profiling = false;
   template <class T>
   T* buf(int which) const {
     return reinterpret_cast<T*>(arena + buf_off[which]);
@@ -316,6 +322,25 @@ int mono_layer_read_buffer(mono_layer_t* h, int which, void* host_dst, size_t by
 
 int mono_layer_launches_per_step(mono_layer_t* h) { return h ? kLaunchesPerStep : MONO_ERR_INVALID_ARG; }
 
+const char* mono_layer_launch_name(int i) {
+  return (i >= 0 && i < kLaunchesPerStep) ? kLaunchNames[i] : nullptr;
+}
+
+int mono_layer_set_profile_events(mono_layer_t* h, void* const* events, int n_events) {
+  if (!h) return MONO_ERR_INVALID_ARG;
+  if (!events) {
+    h->profiling = false;
+    return MONO_OK;
+  }
+  if (n_events != kLaunchesPerStep + 1) return MONO_ERR_INVALID_ARG;
+  for (int i = 0; i < n_events; ++i) {
+    if (!events[i]) return MONO_ERR_INVALID_ARG;
+    h->prof[i] = reinterpret_cast<cudaEvent_t>(events[i]);
+  }
+  h->profiling = true;
+  return MONO_OK;
+}
+
 int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) {
   if (!h || !a) return MONO_ERR_INVALID_ARG;
   const mono_layer_spec& s = h->spec;
@@ -332,16 +357,23 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
       a->kv_stride_block < (int64_t)s.block_size * a->kv_stride_tok)
     return MONO_ERR_BAD_KV_VIEW;
 
-  const Launch L{reinterpret_cast<cudaStream_t>(stream_ptr), true};
+  const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+  const Launch L{stream, !h->profiling};
+  int launch_no = 0;
   const int H = s.hidden, E = s.n_experts, K = s.topk, QW = s.n_q_heads * s.head_dim;
   const int A = s.q_rank + s.kv_dim, G = s.kv_dim / s.head_dim;
   const int nt = nt_bucket(R);
   const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(a->x_in);
   cudaError_t e = cudaSuccess;
-#define RUN(call)                        \
-  do {                                   \
-    e = (call);                          \
-    if (e != cudaSuccess) return cuda_fail(e); \
+#define RUN(call)                                                          \
+  do {                                                                     \
+    if (h->profiling) {                                                    \
+      e = cudaEventRecord(h->prof[launch_no], stream);                     \
+      if (e != cudaSuccess) return cuda_fail(e);                           \
+    }                                                                      \
+    ++launch_no;                                                           \
+    e = (call);                                                            \
+    if (e != cudaSuccess) return cuda_fail(e);                             \
   } while (0)
 
   auto dense = [&](int id, const __half* act, int act_ld, int epi, void* outp, int out_ld,
@@ -507,6 +539,10 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     RUN(launch_final(L, f));
   }
 #undef RUN
+  if (h->profiling) {
+    e = cudaEventRecord(h->prof[kLaunchesPerStep], stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   return MONO_OK;
 }
 
