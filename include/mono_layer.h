@@ -199,6 +199,34 @@ const char *mono_layer_launch_name(int i);
  * until profiling is turned off again with events = NULL. */
 int mono_layer_set_profile_events(mono_layer_t *h, void *const *events, int n_events);
 
+/*
+ * Window attention without any allocation, for callers that cannot call cudaMalloc (for
+ * example code that runs while a CUDA graph is being captured, or a runtime without a
+ * device allocator).  The pages have no counterpart: this is a packaging of the layer's own
+ * split-window attention (launch 5 of a step) whose scratch -- per-split partials, the
+ * combine counters and a status word -- lives in one array compiled into the library,
+ * MONO_NOALLOC_SCRATCH_BYTES on every device that loads it, held until the process exits.
+ *
+ * q: bf16 [rows, n_q_heads * head_dim] (device); o: f16 [rows, n_q_heads * head_dim]
+ * (device, written: each value is the bf16-rounded attention output); the cache view,
+ * positions, row_req and block table as in mono_step_args; only the attention fields of
+ * `spec` are read.  The caller owns every buffer.
+ * Errors: MONO_ERR_TOO_MANY_ROWS when rows > 48 or when rows * n_q_heads * (head_dim + 2)
+ * * 4 bytes times the fewest splits the window allows exceeds the fixed scratch; the other
+ * codes as for a step.  The first call on each device looks the array's device address up
+ * (with that device current) and raises two kernels' shared-memory limits; make that first
+ * call before any stream capture.  Every call shares the one array and clears its counters
+ * and status word on `stream` first: calls whose work overlaps on the GPU (other streams,
+ * other threads) race on it and must be serialised by the caller.  Unmapped pages are
+ * skipped; their status bit is not reported by this entry point.
+ */
+#define MONO_NOALLOC_SCRATCH_BYTES (4u << 20)
+int mono_attention_noalloc(const mono_layer_spec *spec, const void *q, void *o,
+                           const int32_t *positions, const int32_t *row_req,
+                           const int32_t *block_table, int32_t max_blocks, int32_t n_req,
+                           int32_t rows, const uint8_t *kv_cache, int64_t kv_stride_block,
+                           int64_t kv_stride_tok, int64_t kv_num_blocks, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

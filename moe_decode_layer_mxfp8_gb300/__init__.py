@@ -53,7 +53,7 @@ class StepArgs(C.Structure):
 EXPORTS = ["mono_layer_build", "mono_layer_step", "mono_layer_status", "mono_layer_free",
            "mono_layer_strerror", "mono_layer_buffer", "mono_layer_read_buffer",
            "mono_layer_launches_per_step", "mono_layer_launch_name",
-           "mono_layer_set_profile_events"]
+           "mono_layer_set_profile_events", "mono_attention_noalloc"]
 
 _lib = None
 

@@ -22,14 +22,14 @@ def built():
 
 def _declared():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"\b(mono_layer_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(mono_\w+)\s*\(", text)))
 
 
 def test_every_declared_function_is_exported(built):
     names = _declared()
     assert set(names) == set(m.EXPORTS), (names, m.EXPORTS)
     out = subprocess.run(["nm", "-D", "--defined-only", m.LIB_PATH], capture_output=True, text=True).stdout
-    exported = set(re.findall(r"\bT (mono_layer_\w+)", out))
+    exported = set(re.findall(r"\bT (mono_\w+)", out))
     assert set(names) <= exported, set(names) - exported
     for n in names:
         assert hasattr(built, n)
