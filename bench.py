@@ -250,6 +250,7 @@ def kernel_profile(res, dev, reps=20):
             lay.set_profile_events(evs)
         for i in range(reps + 3):
             lay, _ = layers[i % len(layers)]
+            torch.cuda._sleep(2_000_000)  # the GPU waits here while the step is enqueued
             lay.step(step["x"], res["outs"][i % len(layers)], step["positions"], step["row_req"],
                      step["block_table"], step["kv_cache"], stream=stream)
             stream.synchronize()

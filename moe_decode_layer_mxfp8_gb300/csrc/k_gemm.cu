@@ -5,14 +5,14 @@ namespace mono {
 
 namespace {
 
-// Ring depth per variant: two CTAs fit on one SM in every case.
+// Ring depth per variant, chosen so that two or three CTAs fit on one SM.
 template <int FMT, int NT>
 struct Stages;
-template <> struct Stages<8, 1> { static constexpr int value = 8; };
-template <> struct Stages<8, 2> { static constexpr int value = 8; };
-template <> struct Stages<8, 4> { static constexpr int value = 6; };
+template <> struct Stages<8, 1> { static constexpr int value = 6; };
+template <> struct Stages<8, 2> { static constexpr int value = 6; };
+template <> struct Stages<8, 4> { static constexpr int value = 4; };
 template <> struct Stages<8, 6> { static constexpr int value = 4; };
-template <> struct Stages<4, 2> { static constexpr int value = 5; };
+template <> struct Stages<4, 1> { static constexpr int value = 4; };
 
 template <int FMT, int NT>
 constexpr int smem_of() {
@@ -34,11 +34,36 @@ void* variant_kernel(GemmVariant v, int* smem) {
       default: return nullptr;
     }
   }
-  if (v.fmt == 4 && v.nt == 2) {
-    *smem = smem_of<4, 2>();
-    return kernel_of<4, 2>();
+  if (v.fmt == 4 && v.nt == 1) {
+    *smem = smem_of<4, 1>();
+    return kernel_of<4, 1>();
   }
   return nullptr;
+}
+
+cudaLaunchConfig_t config(const Launch& L, int grid, int smem, int cluster,
+                          cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(GEMM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = L.stream;
+  int n = 0;
+  if (L.pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cfg;
 }
 
 }  // namespace
@@ -52,7 +77,9 @@ cudaError_t gemm_prepare(GemmVariant v) {
   int smem = 0;
   void* k = variant_kernel(v, &smem);
   if (!k) return cudaErrorInvalidValue;
-  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
 }
 
 int gemm_ctas_per_sm(GemmVariant v) {
@@ -64,20 +91,35 @@ int gemm_ctas_per_sm(GemmVariant v) {
   return n;
 }
 
+int gemm_max_clusters(GemmVariant v, int cluster) {
+  int smem = 0, n = 0;
+  void* k = variant_kernel(v, &smem);
+  if (!k) return 0;
+  cudaLaunchAttribute attr[2];
+  const Launch L{nullptr, false};
+  cudaLaunchConfig_t cfg = config(L, cluster * 1024, smem, cluster, attr);
+  if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
 cudaError_t launch_gemm(const Launch& L, GemmVariant v, const CUtensorMap& map,
-                        const GemmParams& p, int grid) {
+                        const GemmParams& p, int grid, int cluster) {
   int smem = 0;
   if (!variant_kernel(v, &smem)) return cudaErrorInvalidValue;
-  const dim3 g(grid), b(GEMM_THREADS);
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = config(L, grid, smem, cluster, attr);
   if (v.fmt == 8) {
     switch (v.nt) {
-      case 1: return launch_ex(L, g, b, smem, mx_gemm_kernel<8, 1, Stages<8, 1>::value>, map, p);
-      case 2: return launch_ex(L, g, b, smem, mx_gemm_kernel<8, 2, Stages<8, 2>::value>, map, p);
-      case 4: return launch_ex(L, g, b, smem, mx_gemm_kernel<8, 4, Stages<8, 4>::value>, map, p);
-      default: return launch_ex(L, g, b, smem, mx_gemm_kernel<8, 6, Stages<8, 6>::value>, map, p);
+      case 1: return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<8, 1, Stages<8, 1>::value>, map, p);
+      case 2: return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<8, 2, Stages<8, 2>::value>, map, p);
+      case 4: return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<8, 4, Stages<8, 4>::value>, map, p);
+      default: return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<8, 6, Stages<8, 6>::value>, map, p);
     }
   }
-  return launch_ex(L, g, b, smem, mx_gemm_kernel<4, 2, Stages<4, 2>::value>, map, p);
+  return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<4, 1, Stages<4, 1>::value>, map, p);
 }
 
 }  // namespace mono

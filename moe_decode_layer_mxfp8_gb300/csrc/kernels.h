@@ -112,14 +112,16 @@ cudaError_t launch_router(const Launch&, const RouterArgs&);
 cudaError_t launch_topk(const Launch&, const TopkArgs&);
 cudaError_t launch_final(const Launch&, const FinalArgs&);
 
-// MX GEMM variants: fmt 8 (MXFP8) with nt in {1, 2, 4, 6}; fmt 4 (MXFP4) with nt 2.
+// MX GEMM variants: fmt 8 (MXFP8) with nt in {1, 2, 4, 6}; fmt 4 (MXFP4) with nt 1.
 struct GemmVariant {
   int fmt, nt;
 };
 int gemm_smem_bytes(GemmVariant v);
 cudaError_t gemm_prepare(GemmVariant v);  // raises the dynamic shared-memory limit
 int gemm_ctas_per_sm(GemmVariant v);
+int gemm_max_clusters(GemmVariant v, int cluster);  // co-resident clusters of that size
+// grid must be a multiple of cluster; cluster = p.ksplit for dense matrices, 1 for experts
 cudaError_t launch_gemm(const Launch&, GemmVariant v, const CUtensorMap& map, const GemmParams& p,
-                        int grid);
+                        int grid, int cluster);
 
 }  // namespace mono

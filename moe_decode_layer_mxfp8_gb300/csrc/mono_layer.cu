@@ -34,7 +34,7 @@ struct DensePlan {
   CUtensorMap map;
   const uint8_t* scales;
   int N, K, n_tiles, ksplit, swiglu_I;
-  int* counters;
+  int max_clusters[7];  // co-resident clusters of size ksplit, by activation-tile count nt
 };
 
 }  // namespace
@@ -47,8 +47,6 @@ struct mono_layer {
   size_t arena_bytes = 0;
   size_t buf_off[MONO_BUF_COUNT] = {};
   size_t buf_bytes[MONO_BUF_COUNT] = {};
-  float* ws = nullptr;         // split-K partial tiles
-  int* counters = nullptr;     // split-K counters of every dense plan, then attention counters
   int* attn_counters = nullptr;
   float* attn_part = nullptr;
   int* status = nullptr;
@@ -193,8 +191,6 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
                      {wt->wo_b, wt->wo_b_s, H, s.o_rank, 0},
                      {wt->sh_gu, wt->sh_gu_s, 2 * s.shared_inter, H, s.shared_inter},
                      {wt->sh_d, wt->sh_d_s, H, s.shared_inter, 0}};
-  size_t ws_floats = 0;
-  int total_tiles = 0;
   for (int i = 0; i < D_COUNT; ++i) {
     DensePlan& d = h->dense[i];
     d.scales = defs[i].sc;
@@ -203,10 +199,10 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
     d.swiglu_I = defs[i].swiglu;
     d.n_tiles = d.swiglu_I ? d.swiglu_I / BOX_ROWS : (d.N + TILE_M - 1) / TILE_M;
     const int chunks = d.K / 128;
-    d.ksplit = 1;
-    while (d.n_tiles * d.ksplit < h->num_sms && d.ksplit * 2 <= chunks) d.ksplit *= 2;
-    ws_floats = std::max(ws_floats, (size_t)d.n_tiles * d.ksplit * TILE_M * 48);
-    total_tiles += d.n_tiles;
+    d.ksplit = 1;  // = cluster size: split K until the tiles cover the SMs
+    while (d.n_tiles * d.ksplit < h->num_sms && d.ksplit * 2 <= chunks &&
+           d.ksplit * 2 <= MAX_CLUSTER)
+      d.ksplit *= 2;
     if (!make_map(&d.map, defs[i].w, d.N, d.K)) {
       delete h;
       return MONO_ERR_CUDA;
@@ -238,8 +234,7 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
     h->buf_bytes[b] = sizes[b];
     h->buf_off[b] = take(sizes[b]);
   }
-  const size_t o_ws = take(ws_floats * 4);
-  const size_t o_ctr = take((size_t)(total_tiles + R * G) * 4);
+  const size_t o_ctr = take((size_t)R * G * 4);
   const size_t o_part = take((size_t)R * s.n_q_heads * attn_splits_max * (s.head_dim + 2) * 4);
   const size_t o_status = take(16);
   const size_t o_route = take(sizeof(RouteInfo));
@@ -257,14 +252,7 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
     delete h;
     return cuda_fail(e);
   }
-  h->ws = reinterpret_cast<float*>(h->arena + o_ws);
-  h->counters = reinterpret_cast<int*>(h->arena + o_ctr);
-  int* c = h->counters;
-  for (int i = 0; i < D_COUNT; ++i) {
-    h->dense[i].counters = c;
-    c += h->dense[i].n_tiles;
-  }
-  h->attn_counters = c;
+  h->attn_counters = reinterpret_cast<int*>(h->arena + o_ctr);
   h->attn_part = reinterpret_cast<float*>(h->arena + o_part);
   h->status = reinterpret_cast<int*>(h->arena + o_status);
   h->route = reinterpret_cast<RouteInfo*>(h->arena + o_route);
@@ -274,9 +262,15 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
   for (int nt : {1, 2, 4, 6}) {
     if (gemm_prepare({8, nt}) != cudaSuccess) rc = MONO_ERR_CUDA;
     h->ctas_gemm8[nt] = std::max(1, gemm_ctas_per_sm({8, nt}));
+    for (int i = 0; i < D_COUNT; ++i) {
+      DensePlan& d = h->dense[i];
+      d.max_clusters[nt] = d.ksplit > 1 ? gemm_max_clusters({8, nt}, d.ksplit)
+                                        : h->num_sms * h->ctas_gemm8[nt];
+      if (d.max_clusters[nt] < 1) rc = MONO_ERR_CUDA;
+    }
   }
-  if (gemm_prepare({4, 2}) != cudaSuccess) rc = MONO_ERR_CUDA;
-  h->ctas_gemm4 = std::max(1, gemm_ctas_per_sm({4, 2}));
+  if (gemm_prepare({4, 1}) != cudaSuccess) rc = MONO_ERR_CUDA;
+  h->ctas_gemm4 = std::max(1, gemm_ctas_per_sm({4, 1}));
   if (attention_prepare(s.head_dim) != cudaSuccess) rc = MONO_ERR_CUDA;
   if (rc) {
     (void)cudaGetLastError();
@@ -396,12 +390,9 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     p.resid = resid;
     p.resid_ld = H;
     p.clamp = s.swiglu_clamp;
-    p.ws = h->ws;
-    p.counters = d.counters;
     p.status = h->status;
-    const int items = d.n_tiles * d.ksplit;
-    const int grid = std::min(items, h->num_sms * h->ctas_gemm8[nt]);
-    return launch_gemm(L, {8, nt}, d.map, p, grid);
+    const int clusters = std::min(d.n_tiles, d.max_clusters[nt]);
+    return launch_gemm(L, {8, nt}, d.map, p, clusters * d.ksplit, d.ksplit);
   };
   auto expert = [&](const CUtensorMap& map, const uint8_t* sc, int Kdim, int rows_per_mat,
                     int swiglu, int n_tiles, const __half* act, int act_ld, const int* rowmap,
@@ -418,13 +409,14 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     p.act_rowmap = rowmap;
     p.n_tiles = n_tiles;
     p.ksplit = 1;
+    p.n_slots = R * K;
     p.route = h->route;
     p.epi = epi;
     p.out = outp;
     p.out_ld = out_ld;
     p.clamp = s.swiglu_clamp;
     p.status = h->status;
-    return launch_gemm(L, {4, 2}, map, p, h->num_sms * h->ctas_gemm4);
+    return launch_gemm(L, {4, 1}, map, p, h->num_sms * h->ctas_gemm4, 1);
   };
 
   // ---------------------------------------------------------------- K1: attention front

@@ -6,9 +6,12 @@
 // in place, MXFP8 row-major with 32x32 E8M0 scales, MXFP4 experts).
 //
 // Work item = 64 weight rows (two 32-row TMA boxes) x a K range x up to NT*8 activation
-// rows.  Dense matrices split K across items and reduce the partial tiles in a fixed order
-// (the last-arriving CTA of a tile sums them), so results are bit-reproducible.  Expert
-// matrices take one item per (expert, 64 rows, 16 routed rows) and the full K.
+// rows.  Dense matrices split K over the CTAs of a thread-block cluster: every CTA leaves
+// its partial tile in shared memory, signals its peers through remote mbarriers, and each
+// CTA sums one slice of rows across the cluster's tiles through distributed shared memory
+// in a fixed order -- deterministic and without a global round trip.  Routed experts take
+// one item per (expert, 64 rows, up to 8 routed rows) and the full K; the routing metadata
+// is staged in shared memory once per CTA.
 //
 // CTA = 1 producer warp + 4 consumer warps, persistent over items.  The producer streams
 // weight tiles with cp.async.bulk.tensor (128-byte swizzle) and the activation / scale
@@ -25,13 +28,15 @@
 namespace mono {
 
 constexpr int MAX_EXPERTS = 256;
-constexpr int EXPERT_ROWS = 16;  // routed rows per expert work item
-constexpr int TILE_M = 64;       // weight rows per work item
-constexpr int BOX_ROWS = 32;     // rows per TMA box; two boxes per stage
-constexpr int BOX_BYTES = 128;   // bytes per row per box = the 128-byte swizzle span
+constexpr int MAX_SLOTS = 48 * 8;  // routed (row, slot) pairs of one step at most
+constexpr int EXPERT_ROWS = 8;     // routed rows per expert work item
+constexpr int TILE_M = 64;         // weight rows per work item
+constexpr int BOX_ROWS = 32;       // rows per TMA box; two boxes per stage
+constexpr int BOX_BYTES = 128;     // bytes per row per box = the 128-byte swizzle span
 constexpr int W_STAGE_BYTES = TILE_M * BOX_BYTES;
 constexpr int CONSUMER_WARPS = 4;
 constexpr int GEMM_THREADS = (CONSUMER_WARPS + 1) * 32;
+constexpr int MAX_CLUSTER = 8;
 
 // Routing metadata written by the top-k kernel and read by the expert GEMMs.
 struct RouteInfo {
@@ -40,6 +45,14 @@ struct RouteInfo {
   int hit_off[MAX_EXPERTS];        // first expert-sorted position of its rows
   int hit_cnt[MAX_EXPERTS];        // number of rows routed to it
   int rg_prefix[MAX_EXPERTS + 1];  // prefix sum of ceil(hit_cnt / EXPERT_ROWS)
+};
+
+// Shared-memory copy of the routing metadata plus the activation row map.
+struct RouteSmem {
+  int n_hit;
+  int hit_e[MAX_EXPERTS], hit_off[MAX_EXPERTS], hit_cnt[MAX_EXPERTS];
+  int rg_prefix[MAX_EXPERTS + 1];
+  int rowmap[MAX_SLOTS];
 };
 
 enum : int { EPI_BF16 = 0, EPI_F16 = 1, EPI_RESID_BF16 = 2, EPI_SWIGLU_F16 = 3, EPI_F32 = 4 };
@@ -54,9 +67,10 @@ struct GemmParams {
   const __half* act;      // activations, f16 [*, act_ld]
   int act_ld;
   const int* act_rowmap;  // expert mode: sorted position -> activation row (or null)
+  int n_slots;            // expert mode: entries of act_rowmap
   int dense_rows;         // dense mode: activation rows
   int n_tiles;            // work tiles per matrix
-  int ksplit;             // dense mode: K splits per tile
+  int ksplit;             // dense mode: K splits per tile = cluster size
   const RouteInfo* route; // non-null selects expert mode
   int epi;
   void* out;
@@ -64,8 +78,6 @@ struct GemmParams {
   const __nv_bfloat16* resid;  // EPI_RESID_BF16: added before rounding
   int resid_ld;
   float clamp;                 // EPI_SWIGLU_F16
-  float* ws;                   // split-K partial tiles
-  int* counters;               // split-K arrival counters, one per tile, left at zero
   int* status;
 };
 
@@ -73,9 +85,9 @@ template <int FMT>
 struct FmtTraits;
 template <>
 struct FmtTraits<8> {
-  static constexpr int KC = 128;               // K elements per stage (128 bytes per row)
+  static constexpr int KC = 128;                   // K elements per stage (128 bytes per row)
   static constexpr int ACT_STRIDE = 128 * 2 + 32;  // bytes per activation row (bank spread)
-  static constexpr int SC_BYTES = 8;           // 2 block rows x 4 K blocks
+  static constexpr int SC_BYTES = 8;               // 2 block rows x 4 K blocks
 };
 template <>
 struct FmtTraits<4> {
@@ -88,6 +100,7 @@ __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / 
 
 template <int FMT, int NT, int NSTAGE>
 struct GemmLayout {
+  static constexpr bool EXPERT = FMT == 4;
   static constexpr int ROWS = NT * 8;
   static constexpr int ACT_BYTES = ROWS * FmtTraits<FMT>::ACT_STRIDE;
   static constexpr int SC_BYTES = FmtTraits<FMT>::SC_BYTES;
@@ -96,8 +109,11 @@ struct GemmLayout {
   static constexpr int ACT_OFF = NSTAGE * W_STAGE_BYTES;
   static constexpr int SC_OFF = ACT_OFF + NSTAGE * ACT_BYTES;
   static constexpr int EP_OFF = align_up(SC_OFF + NSTAGE * SC_BYTES, 16);
-  static constexpr int BAR_OFF = align_up(EP_OFF + TILE_M * EP_LD * 4, 16);
-  static constexpr int MISC_OFF = BAR_OFF + 2 * NSTAGE * 8;
+  static constexpr int ROUTE_OFF = align_up(EP_OFF + TILE_M * EP_LD * 4, 16);
+  static constexpr int ROUTE_BYTES = EXPERT ? (int)sizeof(RouteSmem) : 0;
+  static constexpr int BAR_OFF = align_up(ROUTE_OFF + ROUTE_BYTES, 16);
+  // full[NSTAGE], empty[NSTAGE], red_full, red_done
+  static constexpr int MISC_OFF = BAR_OFF + (2 * NSTAGE + 2) * 8;
   static constexpr int BYTES = MISC_OFF + 16 + 1024;  // + slack for 1024-byte alignment
 };
 
@@ -113,25 +129,25 @@ struct Item {
 };
 
 template <int FMT>
-__device__ __forceinline__ void decode_item(const GemmParams& p, int q, Item& it) {
+__device__ __forceinline__ void decode_item(const GemmParams& p, const RouteSmem* rs, int q,
+                                            Item& it) {
   constexpr int KC = FmtTraits<FMT>::KC;
   int base = 0;
-  if (p.route) {
-    const RouteInfo& R = *p.route;
-    int lo = 0, hi = R.n_hit - 1;
+  if (rs) {
+    int lo = 0, hi = rs->n_hit - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (R.rg_prefix[mid] * p.n_tiles <= q) lo = mid; else hi = mid - 1;
+      if (rs->rg_prefix[mid] * p.n_tiles <= q) lo = mid; else hi = mid - 1;
     }
     const int d = lo;
-    const int rgc = R.rg_prefix[d + 1] - R.rg_prefix[d];
-    const int local = q - R.rg_prefix[d] * p.n_tiles;
+    const int rgc = rs->rg_prefix[d + 1] - rs->rg_prefix[d];
+    const int local = q - rs->rg_prefix[d] * p.n_tiles;
     it.tile = local / rgc;
     const int rg = local - it.tile * rgc;
     it.split = 0;
-    base = R.hit_e[d] * p.rows_per_mat;
-    it.n = min(EXPERT_ROWS, R.hit_cnt[d] - rg * EXPERT_ROWS);
-    it.row0 = R.hit_off[d] + rg * EXPERT_ROWS;
+    base = rs->hit_e[d] * p.rows_per_mat;
+    it.n = min(EXPERT_ROWS, rs->hit_cnt[d] - rg * EXPERT_ROWS);
+    it.row0 = rs->hit_off[d] + rg * EXPERT_ROWS;
     it.k0 = 0;
     it.nck = (p.K + KC - 1) / KC;
   } else {
@@ -168,43 +184,52 @@ __device__ __forceinline__ void decode_item(const GemmParams& p, int q, Item& it
   }
 }
 
-__device__ __forceinline__ int total_items(const GemmParams& p) {
-  return p.route ? p.route->rg_prefix[p.route->n_hit] * p.n_tiles : p.n_tiles * p.ksplit;
+__device__ __forceinline__ int total_items(const GemmParams& p, const RouteSmem* rs) {
+  return rs ? rs->rg_prefix[rs->n_hit] * p.n_tiles : p.n_tiles * p.ksplit;
 }
 
-__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(CONSUMER_WARPS * 32)); }
+__device__ __forceinline__ void consumer_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(CONSUMER_WARPS * 32) : "memory");
+}
 
 // Waits on an mbarrier phase; gives up when another warp of the CTA has aborted or the
 // time budget runs out (then raises the status bit and the CTA's abort flag).
+template <bool CLUSTER_ACQUIRE = false>
 __device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity, int* status,
                                           volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto probe = [&]() {
+    return CLUSTER_ACQUIRE ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (probe()) return true;
   const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > WAIT_BUDGET_NS) {
-      atomicOr(status, ST_WAIT_TIMEOUT);
-      *abort = 1;
-      return false;
+  for (uint32_t spin = 1;; ++spin) {
+    if (probe()) return true;
+    if ((spin & 31) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > WAIT_BUDGET_NS) {
+        atomicOr(status, ST_WAIT_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
     }
   }
-  return true;
 }
 
 // ------------------------------------------------------------------------------ producer
 template <int FMT, int NT, int NSTAGE>
-__device__ void gemm_producer(const GemmParams& p, const CUtensorMap* map, uint8_t* smem,
-                              uint64_t* full, uint64_t* empty, volatile int* abort) {
+__device__ void gemm_producer(const GemmParams& p, const RouteSmem* rs, const CUtensorMap* map,
+                              uint8_t* smem, uint64_t* full, uint64_t* empty,
+                              volatile int* abort) {
   using L = GemmLayout<FMT, NT, NSTAGE>;
   constexpr int KC = FmtTraits<FMT>::KC;
   constexpr int ASTR = FmtTraits<FMT>::ACT_STRIDE;
   constexpr int CPR = KC * 2 / 16;  // 16-byte chunks per activation row per stage
   const int lane = threadIdx.x & 31;
-  const int n_items = total_items(p);
+  const int n_items = total_items(p, rs);
   int iter = 0;
   for (int q = blockIdx.x; q < n_items; q += gridDim.x) {
     Item it;
-    decode_item<FMT>(p, q, it);
+    decode_item<FMT>(p, rs, q, it);
     for (int c = 0; c < it.nck; ++c, ++iter) {
       const int s = iter % NSTAGE;
       const uint32_t ph = (iter / NSTAGE) & 1;
@@ -218,7 +243,7 @@ __device__ void gemm_producer(const GemmParams& p, const CUtensorMap* map, uint8
         for (int idx = lane; idx < it.n * CPR; idx += 32) {
           const int i = idx / CPR, ch = idx - i * CPR;
           int arow = i;
-          if (p.route) arow = p.act_rowmap ? p.act_rowmap[it.row0 + i] : it.row0 + i;
+          if (rs) arow = p.act_rowmap ? rs->rowmap[it.row0 + i] : it.row0 + i;
           const bool ok = ch * 16 < vbytes;
           const __half* src = p.act + (long long)arow * p.act_ld + k0 + ch * 8;
           cp_async16(ast + i * ASTR + ch * 16, ok ? (const void*)src : (const void*)p.act,
@@ -275,73 +300,99 @@ __device__ __forceinline__ float swiglu_clamped(float g, float u, float c) {
   return g / (1.0f + expf(-g)) * u;
 }
 
-template <int EP_LD, int ROWS>
-__device__ void gemm_epilogue(const GemmParams& p, const Item& it, float* ep, int tid,
-                              volatile int* flag) {
-  const int n = it.n;
-  if (p.route == nullptr && p.ksplit > 1) {
-    // fixed-order split-K reduction: every split stores its tile, the last one sums them
-    float* ws_tile = p.ws + (size_t)it.tile * p.ksplit * TILE_M * ROWS;
-    float* mine = ws_tile + (size_t)it.split * TILE_M * ROWS;
-    for (int idx = tid; idx < TILE_M * n; idx += CONSUMER_WARPS * 32) {
-      const int i = idx / TILE_M, m = idx - i * TILE_M;
-      mine[m * ROWS + i] = ep[m * EP_LD + i];
-    }
-    __threadfence();
-    consumer_bar();
-    if (tid == 0) *flag = (atomicAdd(&p.counters[it.tile], 1) == p.ksplit - 1);
-    consumer_bar();
-    if (!*flag) return;
-    __threadfence();
-    for (int idx = tid; idx < TILE_M * n; idx += CONSUMER_WARPS * 32) {
-      const int i = idx / TILE_M, m = idx - i * TILE_M;
-      float v = 0.0f;
-      for (int s = 0; s < p.ksplit; ++s) v += __ldcg(ws_tile + ((size_t)s * TILE_M + m) * ROWS + i);
-      ep[m * EP_LD + i] = v;
-    }
-    consumer_bar();
-    if (tid == 0) p.counters[it.tile] = 0;
-  }
+// Stores the finished value of output (row0 + i, col0 + m) -- or, for SwiGLU tiles, of the
+// gate/up pair (m, m + 32) -- according to the epilogue mode.
+__device__ __forceinline__ void epi_store(const GemmParams& p, const Item& it, int m, int i,
+                                          float v, float v_up) {
   if (p.epi == EPI_SWIGLU_F16) {
-    __half* out = reinterpret_cast<__half*>(p.out);
-    for (int idx = tid; idx < BOX_ROWS * n; idx += CONSUMER_WARPS * 32) {
-      const int i = idx / BOX_ROWS, m = idx - i * BOX_ROWS;
-      const int col = it.col0 + m;
-      if (col >= p.swiglu_I) continue;
-      const float t = swiglu_clamped(ep[m * EP_LD + i], ep[(m + BOX_ROWS) * EP_LD + i], p.clamp);
-      out[(size_t)(it.row0 + i) * p.out_ld + col] = bf16_as_f16(t);
-    }
+    const int col = it.col0 + m;
+    if (col >= p.swiglu_I) return;
+    reinterpret_cast<__half*>(p.out)[(size_t)(it.row0 + i) * p.out_ld + col] =
+        bf16_as_f16(swiglu_clamped(v, v_up, p.clamp));
     return;
   }
-  for (int idx = tid; idx < TILE_M * n; idx += CONSUMER_WARPS * 32) {
-    const int i = idx / TILE_M, m = idx - i * TILE_M;
-    const int col = it.col0 + m;
-    if (col >= p.N) continue;
-    const float v = ep[m * EP_LD + i];
-    const size_t o = (size_t)(it.row0 + i) * p.out_ld + col;
-    switch (p.epi) {
-      case EPI_BF16:
-        reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(v);
-        break;
-      case EPI_F16:
-        reinterpret_cast<__half*>(p.out)[o] = bf16_as_f16(v);
-        break;
-      case EPI_RESID_BF16: {
-        const float r = __bfloat162float(p.resid[(size_t)(it.row0 + i) * p.resid_ld + col]);
-        reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(r + v);
-        break;
-      }
-      default:
-        reinterpret_cast<float*>(p.out)[o] = v;
-        break;
+  const int col = it.col0 + m;
+  if (col >= p.N) return;
+  const size_t o = (size_t)(it.row0 + i) * p.out_ld + col;
+  switch (p.epi) {
+    case EPI_BF16:
+      reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(v);
+      break;
+    case EPI_F16:
+      reinterpret_cast<__half*>(p.out)[o] = bf16_as_f16(v);
+      break;
+    case EPI_RESID_BF16: {
+      const float r = __bfloat162float(p.resid[(size_t)(it.row0 + i) * p.resid_ld + col]);
+      reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(r + v);
+      break;
     }
+    default:
+      reinterpret_cast<float*>(p.out)[o] = v;
+      break;
   }
+}
+
+// Epilogue of a tile whose full result sits in this CTA's shared memory.
+template <int EP_LD>
+__device__ void epilogue_local(const GemmParams& p, const Item& it, const float* ep, int tid) {
+  const int n = it.n;
+  const int units = p.epi == EPI_SWIGLU_F16 ? BOX_ROWS : TILE_M;
+  for (int idx = tid; idx < units * n; idx += CONSUMER_WARPS * 32) {
+    const int i = idx / units, m = idx - i * units;
+    const float up = p.epi == EPI_SWIGLU_F16 ? ep[(m + BOX_ROWS) * EP_LD + i] : 0.0f;
+    epi_store(p, it, m, i, ep[m * EP_LD + i], up);
+  }
+}
+
+// Epilogue of a K-split tile: this CTA (rank r of a cluster of ks) sums its slice of the
+// tile's rows over every CTA's partial, in rank order, through distributed shared memory.
+template <int EP_LD>
+__device__ void epilogue_cluster(const GemmParams& p, const Item& it, const float* ep, int tid,
+                                 uint32_t rank, int ks) {
+  const int n = it.n;
+  const bool sw = p.epi == EPI_SWIGLU_F16;
+  const int units = sw ? BOX_ROWS : TILE_M;
+  const int per = units / ks;
+  const int m_lo = (int)rank * per;
+  uint32_t peer[MAX_CLUSTER];
+#pragma unroll
+  for (int r = 0; r < MAX_CLUSTER; ++r) peer[r] = r < ks ? mapa_shared(smem_u32(ep), r) : 0u;
+  for (int idx = tid; idx < per * n; idx += CONSUMER_WARPS * 32) {
+    const int i = idx / per, m = m_lo + (idx - i * per);
+    const uint32_t off = (uint32_t)(m * EP_LD + i) * 4u;
+    const uint32_t off_up = (uint32_t)((m + BOX_ROWS) * EP_LD + i) * 4u;
+    float part[MAX_CLUSTER], part_up[MAX_CLUSTER];
+#pragma unroll
+    for (int r = 0; r < MAX_CLUSTER; ++r) {
+      if (r < ks) {
+        part[r] = ld_dsmem_f32(peer[r] + off);
+        part_up[r] = sw ? ld_dsmem_f32(peer[r] + off_up) : 0.0f;
+      }
+    }
+    float v = 0.0f, v_up = 0.0f;
+#pragma unroll
+    for (int r = 0; r < MAX_CLUSTER; ++r) {
+      if (r < ks) {
+        v += part[r];
+        v_up += part_up[r];
+      }
+    }
+    epi_store(p, it, m, i, v, v_up);
+  }
+}
+
+// E8M0 byte -> 2^(e-127) for e in 1..254 by placing the byte in the f32 exponent field
+// (e = 0 gives 0 instead of 2^-127 and e = 255 infinity instead of NaN; scales of
+// real weights lie far inside that range).
+__device__ __forceinline__ float e8m0_fast(uint32_t word, int byte) {
+  return __uint_as_float(((word >> (8 * byte)) & 0xFFu) << 23);
 }
 
 // ------------------------------------------------------------------------------ consumer
 template <int FMT, int NT, int NSTAGE>
-__device__ void gemm_consumer(const GemmParams& p, uint8_t* smem, uint64_t* full,
-                              uint64_t* empty, volatile int* abort, volatile int* flag) {
+__device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t* smem,
+                              uint64_t* full, uint64_t* empty, uint64_t* red_full,
+                              uint64_t* red_done, volatile int* abort) {
   using L = GemmLayout<FMT, NT, NSTAGE>;
   constexpr int ASTR = FmtTraits<FMT>::ACT_STRIDE;
   const int tid = threadIdx.x;  // 0..127
@@ -349,11 +400,13 @@ __device__ void gemm_consumer(const GemmParams& p, uint8_t* smem, uint64_t* full
   const int g = lane >> 2, c = lane & 3;
   const int r0 = 16 * (w & 1) + g;  // row of this thread inside its 32-row box
   float* ep = reinterpret_cast<float*>(smem + L::EP_OFF);
-  const int n_items = total_items(p);
-  int iter = 0;
+  const int n_items = total_items(p, rs);
+  const bool clustered = rs == nullptr && p.ksplit > 1;
+  const uint32_t rank = clustered ? cluster_ctarank() : 0u;
+  int iter = 0, tiles_done = 0;
   for (int q = blockIdx.x; q < n_items; q += gridDim.x) {
     Item it;
-    decode_item<FMT>(p, q, it);
+    decode_item<FMT>(p, rs, q, it);
     const int ntl = (it.n + 7) >> 3;
     float acc[NT][4];
 #pragma unroll
@@ -378,9 +431,8 @@ __device__ void gemm_consumer(const GemmParams& p, uint8_t* smem, uint64_t* full
           e2m1x8_to_f16x8(lds32(wr1 + off), hb);
           const uint32_t A0[4] = {ha[0], hb[0], ha[1], hb[1]};
           const uint32_t A1[4] = {ha[2], hb[2], ha[3], hb[3]};
-          const uint32_t sa_b = ((b < 4 ? sa8.x : sa8.y) >> (8 * (b & 3))) & 0xFFu;
-          const uint32_t sb_b = ((b < 4 ? sb8.x : sb8.y) >> (8 * (b & 3))) & 0xFFu;
-          const float sa = e8m0_to_f32(sa_b), sb = e8m0_to_f32(sb_b);
+          const float sa = e8m0_fast(b < 4 ? sa8.x : sa8.y, b & 3);
+          const float sb = e8m0_fast(b < 4 ? sb8.x : sb8.y, b & 3);
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
             if (t < ntl) {
@@ -408,7 +460,7 @@ __device__ void gemm_consumer(const GemmParams& p, uint8_t* smem, uint64_t* full
           e4m3x4_to_f16x4(lds32(wr1 + off1), hb1);
           const uint32_t A0[4] = {ha0[0], hb0[0], ha0[1], hb0[1]};
           const uint32_t A1[4] = {ha1[0], hb1[0], ha1[1], hb1[1]};
-          const float sf = e8m0_to_f32((sc4 >> (8 * b)) & 0xFFu);
+          const float sf = e8m0_fast(sc4, b);
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
             if (t < ntl) {
@@ -426,7 +478,10 @@ __device__ void gemm_consumer(const GemmParams& p, uint8_t* smem, uint64_t* full
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    // tile result -> shared memory, then the fused epilogue
+    // K-split tiles: the peers must have finished reading this CTA's previous partial
+    if (clustered && tiles_done > 0 &&
+        !pipe_wait<true>(red_done, (tiles_done - 1) & 1, p.status, abort))
+      return;
     const int m0 = 16 * w + g;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -439,10 +494,26 @@ __device__ void gemm_consumer(const GemmParams& p, uint8_t* smem, uint64_t* full
       }
     }
     if (*abort) return;
-    consumer_bar();
-    gemm_epilogue<L::EP_LD, L::ROWS>(p, it, ep, tid, flag);
-    consumer_bar();
+    if (clustered) {
+      fence_acq_rel_cluster();
+      consumer_bar();
+      if (tid == 0)
+        for (int r = 0; r < p.ksplit; ++r) mbar_arrive_remote(mapa_shared(smem_u32(red_full), r));
+      if (!pipe_wait<true>(red_full, tiles_done & 1, p.status, abort)) return;
+      epilogue_cluster<L::EP_LD>(p, it, ep, tid, rank, p.ksplit);
+      fence_acq_rel_cluster();
+      consumer_bar();
+      if (tid == 0)
+        for (int r = 0; r < p.ksplit; ++r) mbar_arrive_remote(mapa_shared(smem_u32(red_done), r));
+    } else {
+      consumer_bar();
+      epilogue_local<L::EP_LD>(p, it, ep, tid);
+      consumer_bar();
+    }
+    ++tiles_done;
   }
+  // no peer may still be reading this CTA's shared memory when it exits
+  if (clustered && tiles_done > 0) pipe_wait<true>(red_done, (tiles_done - 1) & 1, p.status, abort);
 }
 
 template <int FMT, int NT, int NSTAGE>
@@ -454,25 +525,51 @@ __global__ void __launch_bounds__(GEMM_THREADS)
                                              ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::BAR_OFF);
   uint64_t* empty = full + NSTAGE;
+  uint64_t* red_full = empty + NSTAGE;
+  uint64_t* red_done = red_full + 1;
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::MISC_OFF);
-  volatile int* flag = abort + 1;
   const int warp = threadIdx.x >> 5;
+  const bool clustered = p.route == nullptr && p.ksplit > 1;
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&full[s], 1 + 32);  // expect_tx arrival + one cp.async arrival per lane
       mbar_init(&empty[s], CONSUMER_WARPS);
     }
+    mbar_init(red_full, clustered ? p.ksplit : 1);
+    mbar_init(red_done, clustered ? p.ksplit : 1);
     fence_mbar_init();
     *abort = 0;
   }
   if (warp == CONSUMER_WARPS && (threadIdx.x & 31) == 0) prefetch_tmap(&map);
-  __syncthreads();
+  // every CTA of a cluster must have initialised its barriers before any remote arrival
+  if (clustered)
+    cluster_sync_all();
+  else
+    __syncthreads();
   pdl_trigger();
   pdl_wait();
+  RouteSmem* rs = nullptr;
+  if constexpr (L::EXPERT) {
+    if (p.route) {
+      rs = reinterpret_cast<RouteSmem*>(smem + L::ROUTE_OFF);
+      const int nh = min(p.route->n_hit, MAX_EXPERTS);
+      for (int i = threadIdx.x; i < nh; i += GEMM_THREADS) {
+        rs->hit_e[i] = p.route->hit_e[i];
+        rs->hit_off[i] = p.route->hit_off[i];
+        rs->hit_cnt[i] = p.route->hit_cnt[i];
+      }
+      for (int i = threadIdx.x; i <= nh; i += GEMM_THREADS) rs->rg_prefix[i] = p.route->rg_prefix[i];
+      if (p.act_rowmap)
+        for (int i = threadIdx.x; i < min(p.n_slots, MAX_SLOTS); i += GEMM_THREADS)
+          rs->rowmap[i] = p.act_rowmap[i];
+      if (threadIdx.x == 0) rs->n_hit = nh;
+      __syncthreads();
+    }
+  }
   if (warp == CONSUMER_WARPS)
-    gemm_producer<FMT, NT, NSTAGE>(p, &map, smem, full, empty, abort);
+    gemm_producer<FMT, NT, NSTAGE>(p, rs, &map, smem, full, empty, abort);
   else
-    gemm_consumer<FMT, NT, NSTAGE>(p, smem, full, empty, abort, flag);
+    gemm_consumer<FMT, NT, NSTAGE>(p, rs, smem, full, empty, red_full, red_done, abort);
 }
 
 }  // namespace mono
