@@ -1,0 +1,243 @@
+// Row-wise kernels of the layer: the attention-front and FFN-seam RMSNorms, the q/kv norms
+// with the fp8 KV-cache insert, and the final residual combine ("Mono decode layer for
+// DeepSeek-V4.1-Flash on MI355X", launch table: K1 "q/kv norms, the KV insert", K2 "the FFN
+// seam").  Every thread issues all of its global loads before it uses any of them, so a row
+// costs about one memory latency.
+#include <cuda_fp8.h>
+
+#include "kernels.h"
+
+namespace mono {
+
+namespace {
+
+constexpr int NORM_THREADS = 256;
+constexpr int NORM_CHUNKS = 4;  // 8-element chunks per thread: rows up to 8192 wide
+
+// RMSNorm of one row: y = x / sqrt(mean(x^2) + eps) * gamma, rounded to bf16 and stored as
+// its exact f16 copy for the tensor cores.
+__global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(NormArgs a) {
+  __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
+  const int r = blockIdx.x, tid = threadIdx.x;
+  const __nv_bfloat16* x = a.in + (size_t)r * a.in_ld;
+  uint4 xv[NORM_CHUNKS], gv[NORM_CHUNKS];
+#pragma unroll
+  for (int c = 0; c < NORM_CHUNKS; ++c) {
+    const int i = (c * NORM_THREADS + tid) * 8;
+    if (i < a.dim) {
+      xv[c] = *reinterpret_cast<const uint4*>(x + i);
+      gv[c] = *reinterpret_cast<const uint4*>(a.gamma + i);
+    }
+  }
+  float ss = 0.0f;
+#pragma unroll
+  for (int c = 0; c < NORM_CHUNKS; ++c) {
+    if ((c * NORM_THREADS + tid) * 8 < a.dim) {
+      float f[8];
+      bf16x8_to_f32(xv[c], f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss = fmaf(f[j], f[j], ss);
+    }
+  }
+  ss = block_sum(ss, red);
+  const float inv = 1.0f / sqrtf(ss / (float)a.dim + a.eps);
+  __half* y = a.out + (size_t)r * a.out_ld;
+#pragma unroll
+  for (int c = 0; c < NORM_CHUNKS; ++c) {
+    const int i = (c * NORM_THREADS + tid) * 8;
+    if (i < a.dim) {
+      float f[8], g[8];
+      bf16x8_to_f32(xv[c], f);
+      bf16x8_to_f32(gv[c], g);
+      uint4 o;
+      o.x = pack_f16x2(round_bf16(f[0] * inv * g[0]), round_bf16(f[1] * inv * g[1]));
+      o.y = pack_f16x2(round_bf16(f[2] * inv * g[2]), round_bf16(f[3] * inv * g[3]));
+      o.z = pack_f16x2(round_bf16(f[4] * inv * g[4]), round_bf16(f[5] * inv * g[5]));
+      o.w = pack_f16x2(round_bf16(f[6] * inv * g[6]), round_bf16(f[7] * inv * g[7]));
+      *reinterpret_cast<uint4*>(y + i) = o;
+    }
+  }
+}
+
+// Physical page of token t of request q, or -1 when the block table does not map it.
+__device__ __forceinline__ int page_of(const int* table, int max_blocks, int n_req, long long nb,
+                                       int q, int t, int bs) {
+  const int lb = t / bs;
+  if (q < 0 || q >= n_req || t < 0 || lb >= max_blocks) return -1;
+  const int pb = table[(size_t)q * max_blocks + lb];
+  return (pb < 0 || pb >= nb) ? -1 : pb;
+}
+
+// q-norm and kv-norm of one row, then the fp8 KV insert of the normed kv at the row's
+// position: s = amax / 448 (1 when amax = 0), codes = e4m3(kv / s) rounded to nearest even
+// and saturating, record = codes then s as f32.  Pad rows (position < 0) insert nothing.
+// Thread t owns q chunk t (and t + 256, ...) and kv chunk t: 8 values each.
+constexpr int QKV_CHUNKS = 2;  // q latents up to 4096 wide
+__global__ void __launch_bounds__(NORM_THREADS) qkv_norm_insert_kernel(QkvNormInsertArgs a) {
+  __shared__ float red[32];
+  pdl_trigger();
+  pdl_wait();
+  const int r = blockIdx.x, tid = threadIdx.x;
+  const __nv_bfloat16* row = a.qkv + (size_t)r * (a.q_rank + a.kv_dim);
+  const bool has_kv = tid * 8 < a.kv_dim;  // kv_dim <= 1024: one chunk per thread at most
+  uint4 qv[QKV_CHUNKS], qg[QKV_CHUNKS], kv = {}, kg = {};
+#pragma unroll
+  for (int c = 0; c < QKV_CHUNKS; ++c) {
+    const int i = (c * NORM_THREADS + tid) * 8;
+    if (i < a.q_rank) {
+      qv[c] = *reinterpret_cast<const uint4*>(row + i);
+      qg[c] = *reinterpret_cast<const uint4*>(a.gq + i);
+    }
+  }
+  if (has_kv) {
+    kv = *reinterpret_cast<const uint4*>(row + a.q_rank + tid * 8);
+    kg = *reinterpret_cast<const uint4*>(a.gkv + tid * 8);
+  }
+  const int p = a.positions[r];
+  const int pb = p < 0 ? -1 : page_of(a.block_table, a.max_blocks, a.n_req, a.num_blocks,
+                                     a.row_req[r], p, a.block_size);
+  float ssq = 0.0f, sskv = 0.0f;
+#pragma unroll
+  for (int c = 0; c < QKV_CHUNKS; ++c) {
+    if ((c * NORM_THREADS + tid) * 8 < a.q_rank) {
+      float f[8];
+      bf16x8_to_f32(qv[c], f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ssq = fmaf(f[j], f[j], ssq);
+    }
+  }
+  float kf[8];
+  bf16x8_to_f32(kv, kf);
+  if (has_kv)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sskv = fmaf(kf[j], kf[j], sskv);
+  ssq = block_sum(ssq, red);
+  sskv = block_sum(sskv, red);
+  const float invq = 1.0f / sqrtf(ssq / (float)a.q_rank + a.eps);
+  const float invkv = 1.0f / sqrtf(sskv / (float)a.kv_dim + a.eps);
+#pragma unroll
+  for (int c = 0; c < QKV_CHUNKS; ++c) {
+    const int i = (c * NORM_THREADS + tid) * 8;
+    if (i < a.q_rank) {
+      float f[8], g[8];
+      bf16x8_to_f32(qv[c], f);
+      bf16x8_to_f32(qg[c], g);
+      uint4 o;
+      o.x = pack_f16x2(round_bf16(f[0] * invq * g[0]), round_bf16(f[1] * invq * g[1]));
+      o.y = pack_f16x2(round_bf16(f[2] * invq * g[2]), round_bf16(f[3] * invq * g[3]));
+      o.z = pack_f16x2(round_bf16(f[4] * invq * g[4]), round_bf16(f[5] * invq * g[5]));
+      o.w = pack_f16x2(round_bf16(f[6] * invq * g[6]), round_bf16(f[7] * invq * g[7]));
+      *reinterpret_cast<uint4*>(a.qlatn + (size_t)r * a.q_rank + i) = o;
+    }
+  }
+  float kn[8], g[8];
+  bf16x8_to_f32(kg, g);
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    kn[j] = round_bf16(kf[j] * invkv * g[j]);
+    amax = fmaxf(amax, fabsf(kn[j]));
+  }
+  if (has_kv) {
+    uint4 o;
+    o.x = pack_bf16x2(kn[0], kn[1]);
+    o.y = pack_bf16x2(kn[2], kn[3]);
+    o.z = pack_bf16x2(kn[4], kn[5]);
+    o.w = pack_bf16x2(kn[6], kn[7]);
+    *reinterpret_cast<uint4*>(a.kvn + (size_t)r * a.kv_dim + tid * 8) = o;
+  } else {
+    amax = 0.0f;
+  }
+  amax = block_max(amax, red);
+  if (p < 0) return;
+  if (pb < 0) {
+    if (tid == 0) atomicOr(a.status, ST_UNMAPPED_PAGE);
+    return;
+  }
+  uint8_t* rec = a.cache + (size_t)pb * a.stride_block + (size_t)(p % a.block_size) * a.stride_tok;
+  const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+  if (has_kv) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      w[j] = __nv_cvt_float2_to_fp8x2(make_float2(kn[2 * j] / s, kn[2 * j + 1] / s),
+                                      __NV_SATFINITE, __NV_E4M3);
+    *reinterpret_cast<uint2*>(rec + tid * 8) = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+  }
+  if (tid == 0) *reinterpret_cast<float*>(rec + a.kv_dim) = s;
+}
+
+// out = bf16(h + y_shared + sum_j w_j y_j) in slot order; pad rows copy x.  CTA = one row and
+// FINAL_COLS columns; each thread owns 8 consecutive columns.
+constexpr int FINAL_THREADS = 256;
+constexpr int FINAL_COLS = FINAL_THREADS * 8;
+constexpr int FINAL_MAX_K = 8;
+__global__ void __launch_bounds__(FINAL_THREADS) final_kernel(FinalArgs a) {
+  pdl_trigger();
+  pdl_wait();
+  const int r = blockIdx.x;
+  const int c = blockIdx.y * FINAL_COLS + threadIdx.x * 8;
+  if (c >= a.H) return;
+  const size_t o = (size_t)r * a.H + c;
+  if (a.positions[r] < 0) {
+    *reinterpret_cast<uint4*>(a.out + o) = *reinterpret_cast<const uint4*>(a.x + o);
+    return;
+  }
+  int pos[FINAL_MAX_K];
+  float wj[FINAL_MAX_K];
+#pragma unroll
+  for (int j = 0; j < FINAL_MAX_K; ++j) {
+    pos[j] = j < a.k ? a.slot_pos[r * a.k + j] : -1;
+    wj[j] = j < a.k ? a.topk_w[r * a.k + j] : 0.0f;
+  }
+  const uint4 hv = *reinterpret_cast<const uint4*>(a.h + o);
+  const float4 s0 = *reinterpret_cast<const float4*>(a.ys + o);
+  const float4 s1 = *reinterpret_cast<const float4*>(a.ys + o + 4);
+  float4 y0[FINAL_MAX_K], y1[FINAL_MAX_K];
+#pragma unroll
+  for (int j = 0; j < FINAL_MAX_K; ++j) {
+    if (pos[j] >= 0) {
+      const float* yr = a.yr + (size_t)pos[j] * a.H + c;
+      y0[j] = *reinterpret_cast<const float4*>(yr);
+      y1[j] = *reinterpret_cast<const float4*>(yr + 4);
+    }
+  }
+  float v[8];
+  bf16x8_to_f32(hv, v);
+  v[0] += s0.x, v[1] += s0.y, v[2] += s0.z, v[3] += s0.w;
+  v[4] += s1.x, v[5] += s1.y, v[6] += s1.z, v[7] += s1.w;
+#pragma unroll
+  for (int j = 0; j < FINAL_MAX_K; ++j) {
+    if (pos[j] >= 0) {
+      v[0] = fmaf(wj[j], y0[j].x, v[0]), v[1] = fmaf(wj[j], y0[j].y, v[1]);
+      v[2] = fmaf(wj[j], y0[j].z, v[2]), v[3] = fmaf(wj[j], y0[j].w, v[3]);
+      v[4] = fmaf(wj[j], y1[j].x, v[4]), v[5] = fmaf(wj[j], y1[j].y, v[5]);
+      v[6] = fmaf(wj[j], y1[j].z, v[6]), v[7] = fmaf(wj[j], y1[j].w, v[7]);
+    }
+  }
+  uint4 out;
+  out.x = pack_bf16x2(v[0], v[1]);
+  out.y = pack_bf16x2(v[2], v[3]);
+  out.z = pack_bf16x2(v[4], v[5]);
+  out.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(a.out + o) = out;
+}
+
+}  // namespace
+
+cudaError_t launch_rmsnorm(const Launch& L, const NormArgs& a, int rows) {
+  return launch_ex(L, dim3(rows), dim3(NORM_THREADS), 0, rmsnorm_kernel, a);
+}
+
+cudaError_t launch_qkv_norm_insert(const Launch& L, const QkvNormInsertArgs& a, int rows) {
+  return launch_ex(L, dim3(rows), dim3(NORM_THREADS), 0, qkv_norm_insert_kernel, a);
+}
+
+cudaError_t launch_final(const Launch& L, const FinalArgs& a) {
+  const int ychunks = (a.H + FINAL_COLS - 1) / FINAL_COLS;
+  return launch_ex(L, dim3(a.rows, ychunks), dim3(FINAL_THREADS), 0, final_kernel, a);
+}
+
+}  // namespace mono

@@ -70,15 +70,20 @@ struct AttnArgs {
   int* status;
 };
 
+constexpr int ROUTER_KSLICE = 1024;  // K per router CTA (the router sums partial logits)
+constexpr int ATTN_MAX_SPLITS = 8;   // window splits of the attention at most
+
 struct RouterArgs {
   const __half* u;  // [rows, H]
   const float* wr;  // [E, H]
   int rows, E, H;
-  float* logits;    // [rows, E]
+  float* partial;   // [ceil(H / ROUTER_KSLICE), rows, E]
 };
 
 struct TopkArgs {
-  const float* logits;
+  const float* partial;  // router partials, summed in slice order
+  int kslices;
+  float* logits;         // [rows, E] (for tests)
   const int* positions;
   int rows, E, k;
   float routed_scale;
@@ -109,6 +114,7 @@ cudaError_t launch_qkv_norm_insert(const Launch&, const QkvNormInsertArgs&, int 
 cudaError_t launch_attention(const Launch&, const AttnArgs&, int head_dim, int groups);
 cudaError_t attention_prepare(int head_dim);  // raises the dynamic shared-memory limit
 cudaError_t launch_router(const Launch&, const RouterArgs&);
+cudaError_t router_prepare();  // raises the dynamic shared-memory limit
 cudaError_t launch_topk(const Launch&, const TopkArgs&);
 cudaError_t launch_final(const Launch&, const FinalArgs&);
 

@@ -49,6 +49,11 @@ struct mono_layer {
   size_t buf_bytes[MONO_BUF_COUNT] = {};
   int* attn_counters = nullptr;
   float* attn_part = nullptr;
+  float* router_part = nullptr;
+  int router_kslices = 1;
+  // the shared expert runs on a second stream, concurrently with the router and top-k
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   int* status = nullptr;
   RouteInfo* route = nullptr;
   int* perm = nullptr;
@@ -105,6 +110,7 @@ int check_spec(const mono_layer_spec& s) {
       s.shared_inter % 128)
     return MONO_ERR_UNSUPPORTED_DIMS;
   if (s.kv_dim % 32 || s.kv_dim > 1024) return MONO_ERR_UNSUPPORTED_DIMS;
+  if (s.hidden > 8192 || s.q_rank > 4096) return MONO_ERR_UNSUPPORTED_DIMS;  // row kernels
   if (s.head_dim != 64 && s.head_dim != 128) return MONO_ERR_UNSUPPORTED_DIMS;
   if (s.kv_dim % s.head_dim) return MONO_ERR_UNSUPPORTED_DIMS;
   const int G = s.kv_dim / s.head_dim;
@@ -215,7 +221,7 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
   }
   const int width = std::max(s.causal ? s.window : s.swa_width, s.window);
   h->attn_min_splits = (width + 127) / 128;
-  const int attn_splits_max = std::max(8, h->attn_min_splits);
+  const int attn_splits_max = ATTN_MAX_SPLITS;
 
   // scratch arena
   size_t off = 0;
@@ -239,6 +245,8 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
   const size_t o_status = take(16);
   const size_t o_route = take(sizeof(RouteInfo));
   const size_t o_perm = take((size_t)R * K * 4);
+  h->router_kslices = (H + ROUTER_KSLICE - 1) / ROUTER_KSLICE;
+  const size_t o_rpart = take((size_t)h->router_kslices * R * E * 4);
   h->arena_bytes = off;
   cudaError_t e = cudaMalloc(&h->arena, h->arena_bytes);
   if (e != cudaSuccess) {
@@ -257,6 +265,7 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
   h->status = reinterpret_cast<int*>(h->arena + o_status);
   h->route = reinterpret_cast<RouteInfo*>(h->arena + o_route);
   h->perm = reinterpret_cast<int*>(h->arena + o_perm);
+  h->router_part = reinterpret_cast<float*>(h->arena + o_rpart);
 
   // kernel attributes and occupancy
   for (int nt : {1, 2, 4, 6}) {
@@ -272,10 +281,14 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
   if (gemm_prepare({4, 1}) != cudaSuccess) rc = MONO_ERR_CUDA;
   h->ctas_gemm4 = std::max(1, gemm_ctas_per_sm({4, 1}));
   if (attention_prepare(s.head_dim) != cudaSuccess) rc = MONO_ERR_CUDA;
+  if (router_prepare() != cudaSuccess) rc = MONO_ERR_CUDA;
+  if (!rc && (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
+              cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+              cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess))
+    rc = MONO_ERR_CUDA;
   if (rc) {
     (void)cudaGetLastError();
-    cudaFree(h->arena);
-    delete h;
+    mono_layer_free(h);
     return rc;
   }
   *out = h;
@@ -284,6 +297,9 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
 
 void mono_layer_free(mono_layer_t* h) {
   if (!h) return;
+  if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+  if (h->ev_join) cudaEventDestroy(h->ev_join);
+  if (h->side) cudaStreamDestroy(h->side);
   if (h->arena) cudaFree(h->arena);
   delete h;
 }
@@ -369,9 +385,14 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     e = (call);                                                            \
     if (e != cudaSuccess) return cuda_fail(e);                             \
   } while (0)
+#define RUN_PLAIN(call)                        \
+  do {                                         \
+    e = (call);                                \
+    if (e != cudaSuccess) return cuda_fail(e); \
+  } while (0)
 
   auto dense = [&](int id, const __half* act, int act_ld, int epi, void* outp, int out_ld,
-                   const __nv_bfloat16* resid) {
+                   const __nv_bfloat16* resid, const Launch& LL) {
     const DensePlan& d = h->dense[id];
     GemmParams p = {};
     p.scales = d.scales;
@@ -392,7 +413,7 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     p.clamp = s.swiglu_clamp;
     p.status = h->status;
     const int clusters = std::min(d.n_tiles, d.max_clusters[nt]);
-    return launch_gemm(L, {8, nt}, d.map, p, clusters * d.ksplit, d.ksplit);
+    return launch_gemm(LL, {8, nt}, d.map, p, clusters * d.ksplit, d.ksplit);
   };
   auto expert = [&](const CUtensorMap& map, const uint8_t* sc, int Kdim, int rows_per_mat,
                     int swiglu, int n_tiles, const __half* act, int act_ld, const int* rowmap,
@@ -423,7 +444,7 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
   RUN(launch_rmsnorm(L, {x, H, (const __nv_bfloat16*)h->w.attn_norm, H, s.eps,
                          h->buf<__half>(MONO_BUF_XN), H}, R));
   RUN(dense(D_WQKV, h->buf<__half>(MONO_BUF_XN), H, EPI_BF16, h->buf<void>(MONO_BUF_QKV), A,
-            nullptr));
+            nullptr, L));
   {
     QkvNormInsertArgs q = {};
     q.qkv = h->buf<__nv_bfloat16>(MONO_BUF_QKV);
@@ -448,7 +469,7 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     RUN(launch_qkv_norm_insert(L, q, R));
   }
   RUN(dense(D_WQB, h->buf<__half>(MONO_BUF_QLATN), s.q_rank, EPI_BF16, h->buf<void>(MONO_BUF_Q),
-            QW, nullptr));
+            QW, nullptr, L));
 
   // ---------------------------------------------------------------- K2: attention back
   {
@@ -472,24 +493,46 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     t.stride_tok = a->kv_stride_tok;
     t.num_blocks = a->kv_num_blocks;
     const int want = (2 * h->num_sms + R * G - 1) / (R * G);
-    t.splits = std::max(h->attn_min_splits, std::min(8, want));
+    t.splits = std::max(h->attn_min_splits, std::min(ATTN_MAX_SPLITS, want));
     t.part = h->attn_part;
     t.counters = h->attn_counters;
     t.status = h->status;
     RUN(launch_attention(L, t, s.head_dim, G));
   }
   RUN(dense(D_WOA, h->buf<__half>(MONO_BUF_O), QW, EPI_F16, h->buf<void>(MONO_BUF_OA), s.o_rank,
-            nullptr));
+            nullptr, L));
   RUN(dense(D_WOB, h->buf<__half>(MONO_BUF_OA), s.o_rank, EPI_RESID_BF16, h->buf<void>(MONO_BUF_H),
-            H, x));
+            H, x, L));
 
   // ---------------------------------------------------------------- K2: FFN seam and MoE
   RUN(launch_rmsnorm(L, {h->buf<__nv_bfloat16>(MONO_BUF_H), H, (const __nv_bfloat16*)h->w.ffn_norm,
                          H, s.eps, h->buf<__half>(MONO_BUF_U), H}, R));
-  RUN(launch_router(L, {h->buf<__half>(MONO_BUF_U), h->w.router, R, E, H,
-                        h->buf<float>(MONO_BUF_LOGITS)}));
+  // The shared expert depends only on u: fork it onto the side stream so that it overlaps
+  // the router and the top-k; the routed experts start once both branches are done.  While
+  // profiling, everything stays on one stream in launch-name order.
+  const bool fork = !h->profiling;
+  const Launch Ls{fork ? h->side : stream, !h->profiling};
+  if (fork) {
+    RUN_PLAIN(cudaEventRecord(h->ev_fork, stream));
+    RUN_PLAIN(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
+  }
+  auto shared_expert = [&]() -> int {
+    RUN(dense(D_SHGU, h->buf<__half>(MONO_BUF_U), H, EPI_SWIGLU_F16, h->buf<void>(MONO_BUF_TS),
+              s.shared_inter, nullptr, Ls));
+    RUN(dense(D_SHD, h->buf<__half>(MONO_BUF_TS), s.shared_inter, EPI_F32,
+              h->buf<void>(MONO_BUF_YS), H, nullptr, Ls));
+    return MONO_OK;
+  };
+  if (fork) {
+    const int rs = shared_expert();
+    if (rs != MONO_OK) return rs;
+    RUN_PLAIN(cudaEventRecord(h->ev_join, h->side));
+  }
+  RUN(launch_router(L, {h->buf<__half>(MONO_BUF_U), h->w.router, R, E, H, h->router_part}));
   {
     TopkArgs t = {};
+    t.partial = h->router_part;
+    t.kslices = h->router_kslices;
     t.logits = h->buf<float>(MONO_BUF_LOGITS);
     t.positions = a->positions;
     t.rows = R;
@@ -506,10 +549,12 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     t.status = h->status;
     RUN(launch_topk(L, t));
   }
-  RUN(dense(D_SHGU, h->buf<__half>(MONO_BUF_U), H, EPI_SWIGLU_F16, h->buf<void>(MONO_BUF_TS),
-            s.shared_inter, nullptr));
-  RUN(dense(D_SHD, h->buf<__half>(MONO_BUF_TS), s.shared_inter, EPI_F32, h->buf<void>(MONO_BUF_YS),
-            H, nullptr));
+  if (fork) {
+    RUN_PLAIN(cudaStreamWaitEvent(stream, h->ev_join, 0));
+  } else {
+    const int rs = shared_expert();
+    if (rs != MONO_OK) return rs;
+  }
   RUN(expert(h->map_ex_gu, h->w.ex_gu_s, H, 2 * s.moe_inter, s.moe_inter, s.moe_inter / BOX_ROWS,
              h->buf<__half>(MONO_BUF_U), H, h->perm, EPI_SWIGLU_F16, h->buf<void>(MONO_BUF_TR),
              s.moe_inter));
@@ -531,6 +576,7 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     RUN(launch_final(L, f));
   }
 #undef RUN
+#undef RUN_PLAIN
   if (h->profiling) {
     e = cudaEventRecord(h->prof[kLaunchesPerStep], stream);
     if (e != cudaSuccess) return cuda_fail(e);

@@ -154,3 +154,19 @@ def test_unmapped_page_sets_status_without_fault():
     layer.step(sd["x"], out, sd["positions"], sd["row_req"], sd["block_table"], cache)
     torch.cuda.synchronize()
     assert layer.status() == 0
+
+
+def test_handles_with_different_max_rows_coexist():
+    """Kernel attributes are process-wide: building a small layer after a large one must not
+    break the large one's next step."""
+    _need_gpu()
+    import moe_decode_layer_mxfp8_gb300 as m
+    spec, wn, sn, g, layer, wd, sd = _case("small_r11")
+    small = m.Layer(dict(spec, max_rows=1), wd)
+    out = torch.empty_like(sd["x"])
+    cache = sd["kv_cache"].clone()
+    layer.step(sd["x"], out, sd["positions"], sd["row_req"], sd["block_table"], cache)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert np.array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), g["out"])
+    small.close()
