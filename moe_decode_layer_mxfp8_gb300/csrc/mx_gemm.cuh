@@ -13,12 +13,14 @@
 // one item per (expert, 64 rows, up to 8 routed rows) and the full K; the routing metadata
 // is staged in shared memory once per CTA.
 //
-// CTA = 1 producer warp + 4 consumer warps, persistent over items.  The producer streams
+// CTA = 1 producer warp + 8 consumer warps, persistent over items.  The producer streams
 // weight tiles with cp.async.bulk.tensor (128-byte swizzle) and the activation / scale
-// chunks with cp.async into an NSTAGE ring guarded by mbarriers.  Consumer warp w owns tile
-// rows 16w..16w+15: it decodes its weight fragment in registers (cvt e2m1x2 / e4m3x2 ->
-// f16x2), runs m16n8k16 MMAs per 32-wide K block against every 8-row activation tile, and
-// applies the block's E8M0 scale to the block's f32 result.  Within a 32-wide block the
+// chunks with cp.async into an NSTAGE ring guarded by mbarriers; for dense matrices it
+// issues the first stages' weights before waiting on the previous kernel, so that weight
+// streaming overlaps it.  Consumer warp w owns tile rows 16w..16w+15: it decodes its weight
+// fragment in registers (cvt e2m1x2 / e4m3x2 -> f16x2), runs m16n8k16 MMAs per 32-wide K
+// block against every 8-row activation tile, and applies the block's E8M0 scale to the
+// block's f32 result.  Within a 32-wide block the
 // MMA's 16 K slots are a fixed permutation of the block's K positions, applied to both
 // operands, which leaves the dot product unchanged.
 #pragma once
@@ -34,7 +36,8 @@ constexpr int TILE_M = 64;         // weight rows per work item
 constexpr int BOX_ROWS = 32;       // rows per TMA box; two boxes per stage
 constexpr int BOX_BYTES = 128;     // bytes per row per box = the 128-byte swizzle span
 constexpr int W_STAGE_BYTES = TILE_M * BOX_BYTES;
-constexpr int CONSUMER_WARPS = 4;
+constexpr int CONSUMER_WARPS = 4;  // one per 16-row M-tile (8 would split each stage's K blocks)
+constexpr int KSW = CONSUMER_WARPS / 4;  // warps sharing an M-tile, each taking 1/KSW of the K blocks
 constexpr int GEMM_THREADS = (CONSUMER_WARPS + 1) * 32;
 constexpr int MAX_CLUSTER = 8;
 
@@ -109,7 +112,8 @@ struct GemmLayout {
   static constexpr int ACT_OFF = NSTAGE * W_STAGE_BYTES;
   static constexpr int SC_OFF = ACT_OFF + NSTAGE * ACT_BYTES;
   static constexpr int EP_OFF = align_up(SC_OFF + NSTAGE * SC_BYTES, 16);
-  static constexpr int ROUTE_OFF = align_up(EP_OFF + TILE_M * EP_LD * 4, 16);
+  static constexpr int EP_BYTES = KSW * TILE_M * EP_LD * 4;  // one partial tile per K share
+  static constexpr int ROUTE_OFF = align_up(EP_OFF + EP_BYTES, 16);
   static constexpr int ROUTE_BYTES = EXPERT ? (int)sizeof(RouteSmem) : 0;
   static constexpr int BAR_OFF = align_up(ROUTE_OFF + ROUTE_BYTES, 16);
   // full[NSTAGE], empty[NSTAGE], red_full, red_done
@@ -216,14 +220,90 @@ __device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity, int* s
 }
 
 // ------------------------------------------------------------------------------ producer
+// A stage has two independent halves: the weight tile with its scales (constant data, safe
+// to fetch before the previous kernel has finished) and the activation rows (written by
+// it).  The stage's full barrier counts the TMA bytes, one arrival from lane 0 and one
+// cp.async arrival per lane issued after the activation copies.
 template <int FMT, int NT, int NSTAGE>
-__device__ void gemm_producer(const GemmParams& p, const RouteSmem* rs, const CUtensorMap* map,
-                              uint8_t* smem, uint64_t* full, uint64_t* empty,
-                              volatile int* abort) {
+__device__ __forceinline__ void issue_weights(const GemmParams& p, const CUtensorMap* map,
+                                              uint8_t* smem, uint64_t* full, const Item& it,
+                                              int c, int s, int lane) {
+  using L = GemmLayout<FMT, NT, NSTAGE>;
+  constexpr int KC = FmtTraits<FMT>::KC;
+  const int k0 = it.k0 + c * KC;
+  const int kvalid = min(KC, p.K - k0);
+  uint8_t* sst = smem + L::SC_OFF + s * L::SC_BYTES;
+  const int kb0 = k0 / 32, nkb = kvalid / 32;
+  if (FMT == 8) {
+    if (lane < 2) {
+      const bool ok = lane == 0 ? it.a_ok : it.b_ok;
+      const int row = lane == 0 ? it.sc_a : it.sc_b;
+      const uint8_t* src = p.scales + row * p.scale_ld + kb0;
+      cp_async4(sst + lane * 4, ok ? (const void*)src : (const void*)p.scales,
+                ok ? (uint32_t)min(4, nkb) : 0u);
+    }
+  } else {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const bool ok = half == 0 ? it.a_ok : it.b_ok;
+      const long long row = (long long)(half == 0 ? it.sc_a : it.sc_b) + lane;
+      const uint8_t* src = p.scales + row * p.scale_ld + kb0;
+      uint8_t* dst = sst + (half * BOX_ROWS + lane) * 8;
+      const int n0 = ok ? min(4, nkb) : 0, n1 = ok ? max(0, min(4, nkb - 4)) : 0;
+      cp_async4(dst, n0 ? (const void*)src : (const void*)p.scales, (uint32_t)n0);
+      cp_async4(dst + 4, n1 ? (const void*)(src + 4) : (const void*)p.scales, (uint32_t)n1);
+    }
+  }
+  if (lane == 0) {
+    mbar_arrive_expect_tx(&full[s], W_STAGE_BYTES);
+    const int xb = FMT == 8 ? k0 : k0 / 2;
+    uint8_t* wst = smem + L::W_OFF + s * W_STAGE_BYTES;
+    tma_load_2d(wst, map, xb, it.wrow_a, &full[s]);
+    tma_load_2d(wst + BOX_ROWS * BOX_BYTES, map, xb, it.wrow_b, &full[s]);
+  }
+}
+
+template <int FMT, int NT, int NSTAGE>
+__device__ __forceinline__ void issue_acts(const GemmParams& p, const RouteSmem* rs,
+                                           uint8_t* smem, uint64_t* full, const Item& it, int c,
+                                           int s, int lane) {
   using L = GemmLayout<FMT, NT, NSTAGE>;
   constexpr int KC = FmtTraits<FMT>::KC;
   constexpr int ASTR = FmtTraits<FMT>::ACT_STRIDE;
   constexpr int CPR = KC * 2 / 16;  // 16-byte chunks per activation row per stage
+  const int k0 = it.k0 + c * KC;
+  const int vbytes = min(KC, p.K - k0) * 2;
+  uint8_t* ast = smem + L::ACT_OFF + s * L::ACT_BYTES;
+  for (int idx = lane; idx < it.n * CPR; idx += 32) {
+    const int i = idx / CPR, ch = idx - i * CPR;
+    int arow = i;
+    if (rs) arow = p.act_rowmap ? rs->rowmap[it.row0 + i] : it.row0 + i;
+    const bool ok = ch * 16 < vbytes;
+    const __half* src = p.act + (long long)arow * p.act_ld + k0 + ch * 8;
+    cp_async16(ast + i * ASTR + ch * 16, ok ? (const void*)src : (const void*)p.act,
+               ok ? 16u : 0u);
+  }
+  cp_async_arrive_noinc(&full[s]);
+}
+
+// The first item's first stages whose weights are issued before griddepcontrol.wait (dense
+// matrices only); returns how many.
+template <int FMT, int NT, int NSTAGE>
+__device__ int prefetch_weights(const GemmParams& p, const CUtensorMap* map, uint8_t* smem,
+                                uint64_t* full) {
+  const int lane = threadIdx.x & 31;
+  if (p.route || (int)blockIdx.x >= total_items(p, nullptr)) return 0;
+  Item it;
+  decode_item<FMT>(p, nullptr, blockIdx.x, it);
+  const int pre = min(NSTAGE, it.nck);
+  for (int c = 0; c < pre; ++c) issue_weights<FMT, NT, NSTAGE>(p, map, smem, full, it, c, c, lane);
+  return pre;
+}
+
+template <int FMT, int NT, int NSTAGE>
+__device__ void gemm_producer(const GemmParams& p, const RouteSmem* rs, const CUtensorMap* map,
+                              uint8_t* smem, uint64_t* full, uint64_t* empty,
+                              volatile int* abort, int pre) {
   const int lane = threadIdx.x & 31;
   const int n_items = total_items(p, rs);
   int iter = 0;
@@ -234,54 +314,8 @@ __device__ void gemm_producer(const GemmParams& p, const RouteSmem* rs, const CU
       const int s = iter % NSTAGE;
       const uint32_t ph = (iter / NSTAGE) & 1;
       if (!pipe_wait(&empty[s], ph ^ 1, p.status, abort)) goto drain;
-      {
-        const int k0 = it.k0 + c * KC;
-        const int kvalid = min(KC, p.K - k0);
-        // activations: rows 0..n-1 of this item, zero-filled past K
-        uint8_t* ast = smem + L::ACT_OFF + s * L::ACT_BYTES;
-        const int vbytes = kvalid * 2;
-        for (int idx = lane; idx < it.n * CPR; idx += 32) {
-          const int i = idx / CPR, ch = idx - i * CPR;
-          int arow = i;
-          if (rs) arow = p.act_rowmap ? rs->rowmap[it.row0 + i] : it.row0 + i;
-          const bool ok = ch * 16 < vbytes;
-          const __half* src = p.act + (long long)arow * p.act_ld + k0 + ch * 8;
-          cp_async16(ast + i * ASTR + ch * 16, ok ? (const void*)src : (const void*)p.act,
-                     ok ? 16u : 0u);
-        }
-        // scales of the stage's K blocks
-        uint8_t* sst = smem + L::SC_OFF + s * L::SC_BYTES;
-        const int kb0 = k0 / 32, nkb = kvalid / 32;
-        if (FMT == 8) {
-          if (lane < 2) {
-            const bool ok = lane == 0 ? it.a_ok : it.b_ok;
-            const int row = lane == 0 ? it.sc_a : it.sc_b;
-            const uint8_t* src = p.scales + row * p.scale_ld + kb0;
-            cp_async4(sst + lane * 4, ok ? (const void*)src : (const void*)p.scales,
-                      ok ? (uint32_t)min(4, nkb) : 0u);
-          }
-        } else {
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const bool ok = half == 0 ? it.a_ok : it.b_ok;
-            const long long row = (long long)(half == 0 ? it.sc_a : it.sc_b) + lane;
-            const uint8_t* src = p.scales + row * p.scale_ld + kb0;
-            uint8_t* dst = sst + (half * BOX_ROWS + lane) * 8;
-            const int n0 = ok ? min(4, nkb) : 0, n1 = ok ? max(0, min(4, nkb - 4)) : 0;
-            cp_async4(dst, n0 ? (const void*)src : (const void*)p.scales, (uint32_t)n0);
-            cp_async4(dst + 4, n1 ? (const void*)(src + 4) : (const void*)p.scales, (uint32_t)n1);
-          }
-        }
-        cp_async_arrive_noinc(&full[s]);
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[s], W_STAGE_BYTES);
-          const int xb = FMT == 8 ? k0 : k0 / 2;
-          uint8_t* wst = smem + L::W_OFF + s * W_STAGE_BYTES;
-          tma_load_2d(wst, map, xb, it.wrow_a, &full[s]);
-          tma_load_2d(wst + BOX_ROWS * BOX_BYTES, map, xb, it.wrow_b, &full[s]);
-        }
-      }
+      if (iter >= pre) issue_weights<FMT, NT, NSTAGE>(p, map, smem, full, it, c, s, lane);
+      issue_acts<FMT, NT, NSTAGE>(p, rs, smem, full, it, c, s, lane);
     }
   }
   return;
@@ -385,7 +419,7 @@ __device__ void epilogue_cluster(const GemmParams& p, const Item& it, const floa
 // (e = 0 gives 0 instead of 2^-127 and e = 255 infinity instead of NaN; scales of
 // real weights lie far inside that range).
 __device__ __forceinline__ float e8m0_fast(uint32_t word, int byte) {
-  return __uint_as_float(((word >> (8 * byte)) & 0xFFu) << 23);
+  return __uint_as_float(__byte_perm(word, 0u, 0x4440u + byte) << 23);
 }
 
 // ------------------------------------------------------------------------------ consumer
@@ -395,11 +429,20 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
                               uint64_t* red_done, volatile int* abort) {
   using L = GemmLayout<FMT, NT, NSTAGE>;
   constexpr int ASTR = FmtTraits<FMT>::ACT_STRIDE;
-  const int tid = threadIdx.x;  // 0..127
+  constexpr int NB = FmtTraits<FMT>::KC / 32;  // 32-wide K blocks per stage
+  constexpr int HB = NB / KSW;                 // blocks per K share
+  const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
+  const int mt = w & 3, kh = w >> 2;           // M-tile and K-half of this warp
   const int g = lane >> 2, c = lane & 3;
-  const int r0 = 16 * (w & 1) + g;  // row of this thread inside its 32-row box
+  const int r0 = 16 * (mt & 1) + g;            // row of this thread inside its 32-row box
   float* ep = reinterpret_cast<float*>(smem + L::EP_OFF);
+  float* ep_mine = ep + kh * (TILE_M * L::EP_LD);
+  // swizzled word offsets of this thread's K blocks (fmt 4: one chunk a block; fmt 8: two)
+  int offs[FMT == 4 ? HB : 2 * HB];
+#pragma unroll
+  for (int j = 0; j < (FMT == 4 ? HB : 2 * HB); ++j)
+    offs[j] = (((FMT == 4 ? kh * HB : 2 * kh * HB) + j) ^ g) * 16 + c * 4;
   const int n_items = total_items(p, rs);
   const bool clustered = rs == nullptr && p.ksplit > 1;
   const uint32_t rank = clustered ? cluster_ctarank() : 0u;
@@ -415,62 +458,78 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
     for (int ck = 0; ck < it.nck; ++ck, ++iter) {
       const int s = iter % NSTAGE;
       if (!pipe_wait(&full[s], (iter / NSTAGE) & 1, p.status, abort)) return;
-      const uint8_t* wbox = smem + L::W_OFF + s * W_STAGE_BYTES + (w >> 1) * (BOX_ROWS * BOX_BYTES);
+      const uint8_t* wbox = smem + L::W_OFF + s * W_STAGE_BYTES + (mt >> 1) * (BOX_ROWS * BOX_BYTES);
       const uint8_t* wr0 = wbox + r0 * BOX_BYTES;
       const uint8_t* wr1 = wr0 + 8 * BOX_BYTES;
       const uint8_t* sc = smem + L::SC_OFF + s * L::SC_BYTES;
       const uint8_t* act = smem + L::ACT_OFF + s * L::ACT_BYTES + g * ASTR;
       if (FMT == 4) {
-        const uint2 sa8 = lds64(sc + (16 * w + g) * 8);
-        const uint2 sb8 = lds64(sc + (16 * w + g + 8) * 8);
+        uint32_t sa[HB / 4], sb[HB / 4];
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          const int off = ((b ^ g) << 4) + (c << 2);
+        for (int j = 0; j < HB / 4; ++j) {
+          sa[j] = lds32(sc + (16 * mt + g) * 8 + 4 * (kh * HB / 4 + j));
+          sb[j] = lds32(sc + (16 * mt + g + 8) * 8 + 4 * (kh * HB / 4 + j));
+        }
+        uint32_t wa[HB], wb[HB];
+#pragma unroll
+        for (int j = 0; j < HB; ++j) {  // all of this warp's weight words first
+          wa[j] = lds32(wr0 + offs[j]);
+          wb[j] = lds32(wr1 + offs[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < HB; ++j) {
+          const int b = kh * HB + j;
           uint32_t ha[4], hb[4];
-          e2m1x8_to_f16x8(lds32(wr0 + off), ha);
-          e2m1x8_to_f16x8(lds32(wr1 + off), hb);
+          e2m1x8_to_f16x8(wa[j], ha);
+          e2m1x8_to_f16x8(wb[j], hb);
           const uint32_t A0[4] = {ha[0], hb[0], ha[1], hb[1]};
           const uint32_t A1[4] = {ha[2], hb[2], ha[3], hb[3]};
-          const float sa = e8m0_fast(b < 4 ? sa8.x : sa8.y, b & 3);
-          const float sb = e8m0_fast(b < 4 ? sb8.x : sb8.y, b & 3);
+          const float fa = e8m0_fast(sa[j / 4], j % 4), fb = e8m0_fast(sb[j / 4], j % 4);
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
-            if (t < ntl) {
+            if (NT == 1 || t < ntl) {
               const uint4 bv = lds128(act + t * 8 * ASTR + (32 * b + 8 * c) * 2);
               float d[4];
               mma_f16(d, A0, bv.x, bv.y);
               mma_f16_acc(d, A1, bv.z, bv.w);
-              acc[t][0] = fmaf(sa, d[0], acc[t][0]);
-              acc[t][1] = fmaf(sa, d[1], acc[t][1]);
-              acc[t][2] = fmaf(sb, d[2], acc[t][2]);
-              acc[t][3] = fmaf(sb, d[3], acc[t][3]);
+              acc[t][0] = fmaf(fa, d[0], acc[t][0]);
+              acc[t][1] = fmaf(fa, d[1], acc[t][1]);
+              acc[t][2] = fmaf(fb, d[2], acc[t][2]);
+              acc[t][3] = fmaf(fb, d[3], acc[t][3]);
             }
           }
         }
       } else {
-        const uint32_t sc4 = lds32(sc + (w >> 1) * 4);
+        const uint32_t sc4 = lds32(sc + (mt >> 1) * 4);
+        uint32_t wa0[HB], wb0[HB], wa1[HB], wb1[HB];
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const int off0 = (((2 * b) ^ g) << 4) + (c << 2);
-          const int off1 = (((2 * b + 1) ^ g) << 4) + (c << 2);
+        for (int j = 0; j < HB; ++j) {
+          wa0[j] = lds32(wr0 + offs[2 * j]);
+          wb0[j] = lds32(wr1 + offs[2 * j]);
+          wa1[j] = lds32(wr0 + offs[2 * j + 1]);
+          wb1[j] = lds32(wr1 + offs[2 * j + 1]);
+        }
+#pragma unroll
+        for (int j = 0; j < HB; ++j) {
+          const int b = kh * HB + j;
           uint32_t ha0[2], hb0[2], ha1[2], hb1[2];
-          e4m3x4_to_f16x4(lds32(wr0 + off0), ha0);
-          e4m3x4_to_f16x4(lds32(wr1 + off0), hb0);
-          e4m3x4_to_f16x4(lds32(wr0 + off1), ha1);
-          e4m3x4_to_f16x4(lds32(wr1 + off1), hb1);
+          e4m3x4_to_f16x4(wa0[j], ha0);
+          e4m3x4_to_f16x4(wb0[j], hb0);
+          e4m3x4_to_f16x4(wa1[j], ha1);
+          e4m3x4_to_f16x4(wb1[j], hb1);
           const uint32_t A0[4] = {ha0[0], hb0[0], ha0[1], hb0[1]};
           const uint32_t A1[4] = {ha1[0], hb1[0], ha1[1], hb1[1]};
           const float sf = e8m0_fast(sc4, b);
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
-            if (t < ntl) {
+            if (NT == 1 || t < ntl) {
               const uint2 b0 = lds64(act + t * 8 * ASTR + (32 * b + 4 * c) * 2);
               const uint2 b1 = lds64(act + t * 8 * ASTR + (32 * b + 16 + 4 * c) * 2);
               float d[4];
               mma_f16(d, A0, b0.x, b0.y);
               mma_f16_acc(d, A1, b1.x, b1.y);
 #pragma unroll
-              for (int j = 0; j < 4; ++j) acc[t][j] = fmaf(sf, d[j], acc[t][j]);
+              for (int jj = 0; jj < 4; ++jj) acc[t][jj] = fmaf(sf, d[jj], acc[t][jj]);
             }
           }
         }
@@ -482,18 +541,26 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
     if (clustered && tiles_done > 0 &&
         !pipe_wait<true>(red_done, (tiles_done - 1) & 1, p.status, abort))
       return;
-    const int m0 = 16 * w + g;
+    const int m0 = 16 * mt + g;
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      if (t < ntl) {
+      if (NT == 1 || t < ntl) {
         const int col = t * 8 + 2 * c;
-        ep[m0 * L::EP_LD + col] = acc[t][0];
-        ep[m0 * L::EP_LD + col + 1] = acc[t][1];
-        ep[(m0 + 8) * L::EP_LD + col] = acc[t][2];
-        ep[(m0 + 8) * L::EP_LD + col + 1] = acc[t][3];
+        ep_mine[m0 * L::EP_LD + col] = acc[t][0];
+        ep_mine[m0 * L::EP_LD + col + 1] = acc[t][1];
+        ep_mine[(m0 + 8) * L::EP_LD + col] = acc[t][2];
+        ep_mine[(m0 + 8) * L::EP_LD + col + 1] = acc[t][3];
       }
     }
     if (*abort) return;
+    if (KSW > 1) {  // the K shares' tiles, added in a fixed order
+      consumer_bar();
+      const int cols = ntl * 8;
+      for (int idx = tid; idx < TILE_M * cols; idx += CONSUMER_WARPS * 32) {
+        const int m = idx / cols, col = idx - m * cols;
+        for (int k = 1; k < KSW; ++k) ep[m * L::EP_LD + col] += ep[k * TILE_M * L::EP_LD + m * L::EP_LD + col];
+      }
+    }
     if (clustered) {
       fence_acq_rel_cluster();
       consumer_bar();
@@ -547,6 +614,9 @@ __global__ void __launch_bounds__(GEMM_THREADS)
   else
     __syncthreads();
   pdl_trigger();
+  // weights do not depend on the previous kernel: start streaming them before waiting on it
+  int pre = 0;
+  if (warp == CONSUMER_WARPS) pre = prefetch_weights<FMT, NT, NSTAGE>(p, &map, smem, full);
   pdl_wait();
   RouteSmem* rs = nullptr;
   if constexpr (L::EXPERT) {
@@ -567,7 +637,7 @@ __global__ void __launch_bounds__(GEMM_THREADS)
     }
   }
   if (warp == CONSUMER_WARPS)
-    gemm_producer<FMT, NT, NSTAGE>(p, rs, &map, smem, full, empty, abort);
+    gemm_producer<FMT, NT, NSTAGE>(p, rs, &map, smem, full, empty, abort, pre);
   else
     gemm_consumer<FMT, NT, NSTAGE>(p, rs, smem, full, empty, red_full, red_done, abort);
 }
