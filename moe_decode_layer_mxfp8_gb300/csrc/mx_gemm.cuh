@@ -36,9 +36,9 @@ constexpr int TILE_M = 64;         // weight rows per work item
 constexpr int BOX_ROWS = 32;       // rows per TMA box; two boxes per stage
 constexpr int BOX_BYTES = 128;     // bytes per row per box = the 128-byte swizzle span
 constexpr int W_STAGE_BYTES = TILE_M * BOX_BYTES;
-constexpr int CONSUMER_WARPS = 4;  // one per 16-row M-tile (8 would split each stage's K blocks)
-constexpr int KSW = CONSUMER_WARPS / 4;  // warps sharing an M-tile, each taking 1/KSW of the K blocks
-constexpr int GEMM_THREADS = (CONSUMER_WARPS + 1) * 32;
+// Threads of a CTA whose consumers are 4 M-tile warps times KS K-shares (the KS warps of an
+// M-tile each take 1/KS of every stage's K blocks), plus the producer warp.
+__host__ __device__ constexpr int gemm_threads(int ks) { return (4 * ks + 1) * 32; }
 constexpr int MAX_CLUSTER = 8;
 
 // Routing metadata written by the top-k kernel and read by the expert GEMMs.
@@ -101,7 +101,7 @@ struct FmtTraits<4> {
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
-template <int FMT, int NT, int NSTAGE>
+template <int FMT, int NT, int NSTAGE, int KS>
 struct GemmLayout {
   static constexpr bool EXPERT = FMT == 4;
   static constexpr int ROWS = NT * 8;
@@ -112,7 +112,7 @@ struct GemmLayout {
   static constexpr int ACT_OFF = NSTAGE * W_STAGE_BYTES;
   static constexpr int SC_OFF = ACT_OFF + NSTAGE * ACT_BYTES;
   static constexpr int EP_OFF = align_up(SC_OFF + NSTAGE * SC_BYTES, 16);
-  static constexpr int EP_BYTES = KSW * TILE_M * EP_LD * 4;  // one partial tile per K share
+  static constexpr int EP_BYTES = KS * TILE_M * EP_LD * 4;  // one partial tile per K share
   static constexpr int ROUTE_OFF = align_up(EP_OFF + EP_BYTES, 16);
   static constexpr int ROUTE_BYTES = EXPERT ? (int)sizeof(RouteSmem) : 0;
   static constexpr int BAR_OFF = align_up(ROUTE_OFF + ROUTE_BYTES, 16);
@@ -192,8 +192,9 @@ __device__ __forceinline__ int total_items(const GemmParams& p, const RouteSmem*
   return rs ? rs->rg_prefix[rs->n_hit] * p.n_tiles : p.n_tiles * p.ksplit;
 }
 
+template <int NTHR>
 __device__ __forceinline__ void consumer_bar() {
-  asm volatile("bar.sync 1, %0;" ::"n"(CONSUMER_WARPS * 32) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(NTHR) : "memory");
 }
 
 // Waits on an mbarrier phase; gives up when another warp of the CTA has aborted or the
@@ -224,11 +225,11 @@ __device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity, int* s
 // to fetch before the previous kernel has finished) and the activation rows (written by
 // it).  The stage's full barrier counts the TMA bytes, one arrival from lane 0 and one
 // cp.async arrival per lane issued after the activation copies.
-template <int FMT, int NT, int NSTAGE>
+template <int FMT, int NT, int NSTAGE, int KS>
 __device__ __forceinline__ void issue_weights(const GemmParams& p, const CUtensorMap* map,
                                               uint8_t* smem, uint64_t* full, const Item& it,
                                               int c, int s, int lane) {
-  using L = GemmLayout<FMT, NT, NSTAGE>;
+  using L = GemmLayout<FMT, NT, NSTAGE, KS>;
   constexpr int KC = FmtTraits<FMT>::KC;
   const int k0 = it.k0 + c * KC;
   const int kvalid = min(KC, p.K - k0);
@@ -263,11 +264,11 @@ __device__ __forceinline__ void issue_weights(const GemmParams& p, const CUtenso
   }
 }
 
-template <int FMT, int NT, int NSTAGE>
+template <int FMT, int NT, int NSTAGE, int KS>
 __device__ __forceinline__ void issue_acts(const GemmParams& p, const RouteSmem* rs,
                                            uint8_t* smem, uint64_t* full, const Item& it, int c,
                                            int s, int lane) {
-  using L = GemmLayout<FMT, NT, NSTAGE>;
+  using L = GemmLayout<FMT, NT, NSTAGE, KS>;
   constexpr int KC = FmtTraits<FMT>::KC;
   constexpr int ASTR = FmtTraits<FMT>::ACT_STRIDE;
   constexpr int CPR = KC * 2 / 16;  // 16-byte chunks per activation row per stage
@@ -288,7 +289,7 @@ __device__ __forceinline__ void issue_acts(const GemmParams& p, const RouteSmem*
 
 // The first item's first stages whose weights are issued before griddepcontrol.wait (dense
 // matrices only); returns how many.
-template <int FMT, int NT, int NSTAGE>
+template <int FMT, int NT, int NSTAGE, int KS>
 __device__ int prefetch_weights(const GemmParams& p, const CUtensorMap* map, uint8_t* smem,
                                 uint64_t* full) {
   const int lane = threadIdx.x & 31;
@@ -296,11 +297,11 @@ __device__ int prefetch_weights(const GemmParams& p, const CUtensorMap* map, uin
   Item it;
   decode_item<FMT>(p, nullptr, blockIdx.x, it);
   const int pre = min(NSTAGE, it.nck);
-  for (int c = 0; c < pre; ++c) issue_weights<FMT, NT, NSTAGE>(p, map, smem, full, it, c, c, lane);
+  for (int c = 0; c < pre; ++c) issue_weights<FMT, NT, NSTAGE, KS>(p, map, smem, full, it, c, c, lane);
   return pre;
 }
 
-template <int FMT, int NT, int NSTAGE>
+template <int FMT, int NT, int NSTAGE, int KS>
 __device__ void gemm_producer(const GemmParams& p, const RouteSmem* rs, const CUtensorMap* map,
                               uint8_t* smem, uint64_t* full, uint64_t* empty,
                               volatile int* abort, int pre) {
@@ -314,8 +315,8 @@ __device__ void gemm_producer(const GemmParams& p, const RouteSmem* rs, const CU
       const int s = iter % NSTAGE;
       const uint32_t ph = (iter / NSTAGE) & 1;
       if (!pipe_wait(&empty[s], ph ^ 1, p.status, abort)) goto drain;
-      if (iter >= pre) issue_weights<FMT, NT, NSTAGE>(p, map, smem, full, it, c, s, lane);
-      issue_acts<FMT, NT, NSTAGE>(p, rs, smem, full, it, c, s, lane);
+      if (iter >= pre) issue_weights<FMT, NT, NSTAGE, KS>(p, map, smem, full, it, c, s, lane);
+      issue_acts<FMT, NT, NSTAGE, KS>(p, rs, smem, full, it, c, s, lane);
     }
   }
   return;
@@ -334,55 +335,77 @@ __device__ __forceinline__ float swiglu_clamped(float g, float u, float c) {
   return g / (1.0f + expf(-g)) * u;
 }
 
-// Stores the finished value of output (row0 + i, col0 + m) -- or, for SwiGLU tiles, of the
-// gate/up pair (m, m + 32) -- according to the epilogue mode.
-__device__ __forceinline__ void epi_store(const GemmParams& p, const Item& it, int m, int i,
-                                          float v, float v_up) {
-  if (p.epi == EPI_SWIGLU_F16) {
-    const int col = it.col0 + m;
-    if (col >= p.swiglu_I) return;
-    reinterpret_cast<__half*>(p.out)[(size_t)(it.row0 + i) * p.out_ld + col] =
-        bf16_as_f16(swiglu_clamped(v, v_up, p.clamp));
-    return;
-  }
-  const int col = it.col0 + m;
-  if (col >= p.N) return;
-  const size_t o = (size_t)(it.row0 + i) * p.out_ld + col;
-  switch (p.epi) {
-    case EPI_BF16:
-      reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(v);
-      break;
-    case EPI_F16:
-      reinterpret_cast<__half*>(p.out)[o] = bf16_as_f16(v);
-      break;
-    case EPI_RESID_BF16: {
-      const float r = __bfloat162float(p.resid[(size_t)(it.row0 + i) * p.resid_ld + col]);
-      reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(r + v);
-      break;
+// Writes finished tile values to the output.  fin[m * EP_LD + i] holds the value of output
+// row (row0 + i), column (col0 + m) -- for SwiGLU tiles the already combined gate/up value --
+// for m in [m_lo, m_lo + per).  Four values per thread are in flight at a time, their
+// residual reads issued before any store.
+template <int EP_LD, int NTHR>
+__device__ void store_rows(const GemmParams& p, const Item& it, const float* fin, int m_lo,
+                           int per, int tid) {
+  const int total = per * it.n;
+  const bool sw = p.epi == EPI_SWIGLU_F16;
+  const int ncols = sw ? p.swiglu_I : p.N;
+  for (int base = tid; base < total; base += 4 * NTHR) {
+    float v[4], r[4];
+    size_t o[4];
+    bool ok[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = base + u * NTHR;
+      const int i = idx / per, m = m_lo + (idx - (idx / per) * per);
+      const int col = it.col0 + m;
+      ok[u] = idx < total && col < ncols;
+      o[u] = (size_t)(it.row0 + i) * p.out_ld + col;
+      v[u] = ok[u] ? fin[m * EP_LD + i] : 0.0f;
+      r[u] = ok[u] && p.epi == EPI_RESID_BF16
+                 ? __bfloat162float(p.resid[(size_t)(it.row0 + i) * p.resid_ld + col])
+                 : 0.0f;
     }
-    default:
-      reinterpret_cast<float*>(p.out)[o] = v;
-      break;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (!ok[u]) continue;
+      switch (p.epi) {
+        case EPI_BF16:
+          reinterpret_cast<__nv_bfloat16*>(p.out)[o[u]] = __float2bfloat16_rn(v[u]);
+          break;
+        case EPI_F16:
+        case EPI_SWIGLU_F16:
+          reinterpret_cast<__half*>(p.out)[o[u]] = bf16_as_f16(v[u]);
+          break;
+        case EPI_RESID_BF16:
+          reinterpret_cast<__nv_bfloat16*>(p.out)[o[u]] = __float2bfloat16_rn(r[u] + v[u]);
+          break;
+        default:
+          reinterpret_cast<float*>(p.out)[o[u]] = v[u];
+          break;
+      }
+    }
   }
 }
 
-// Epilogue of a tile whose full result sits in this CTA's shared memory.
-template <int EP_LD>
-__device__ void epilogue_local(const GemmParams& p, const Item& it, const float* ep, int tid) {
-  const int n = it.n;
-  const int units = p.epi == EPI_SWIGLU_F16 ? BOX_ROWS : TILE_M;
-  for (int idx = tid; idx < units * n; idx += CONSUMER_WARPS * 32) {
-    const int i = idx / units, m = idx - i * units;
-    const float up = p.epi == EPI_SWIGLU_F16 ? ep[(m + BOX_ROWS) * EP_LD + i] : 0.0f;
-    epi_store(p, it, m, i, ep[m * EP_LD + i], up);
+// Epilogue of a tile whose full result sits in this CTA's shared memory.  SwiGLU tiles first
+// combine each gate row m with its up row m + 32 in place.
+template <int EP_LD, int NTHR>
+__device__ void epilogue_local(const GemmParams& p, const Item& it, float* ep, int tid) {
+  const bool sw = p.epi == EPI_SWIGLU_F16;
+  if (sw) {
+    for (int idx = tid; idx < BOX_ROWS * it.n; idx += NTHR) {
+      const int i = idx / BOX_ROWS, m = idx - i * BOX_ROWS;
+      ep[m * EP_LD + i] = swiglu_clamped(ep[m * EP_LD + i], ep[(m + BOX_ROWS) * EP_LD + i], p.clamp);
+    }
+    consumer_bar<NTHR>();
   }
+  store_rows<EP_LD, NTHR>(p, it, ep, 0, sw ? BOX_ROWS : TILE_M, tid);
 }
 
 // Epilogue of a K-split tile: this CTA (rank r of a cluster of ks) sums its slice of the
-// tile's rows over every CTA's partial, in rank order, through distributed shared memory.
-template <int EP_LD>
-__device__ void epilogue_cluster(const GemmParams& p, const Item& it, const float* ep, int tid,
-                                 uint32_t rank, int ks) {
+// tile's rows over every CTA's partial, in rank order, through distributed shared memory,
+// and keeps the sums in its own partial's slice (rows no peer reads).  Once every consumer
+// thread has its sums, the CTA tells each peer that it is done reading the peer's partial,
+// then writes the slice out.
+template <int EP_LD, int NTHR>
+__device__ void epilogue_cluster(const GemmParams& p, const Item& it, float* ep, int tid,
+                                 uint32_t rank, int ks, uint64_t* red_done) {
   const int n = it.n;
   const bool sw = p.epi == EPI_SWIGLU_F16;
   const int units = sw ? BOX_ROWS : TILE_M;
@@ -391,7 +414,7 @@ __device__ void epilogue_cluster(const GemmParams& p, const Item& it, const floa
   uint32_t peer[MAX_CLUSTER];
 #pragma unroll
   for (int r = 0; r < MAX_CLUSTER; ++r) peer[r] = r < ks ? mapa_shared(smem_u32(ep), r) : 0u;
-  for (int idx = tid; idx < per * n; idx += CONSUMER_WARPS * 32) {
+  for (int idx = tid; idx < per * n; idx += NTHR) {
     const int i = idx / per, m = m_lo + (idx - i * per);
     const uint32_t off = (uint32_t)(m * EP_LD + i) * 4u;
     const uint32_t off_up = (uint32_t)((m + BOX_ROWS) * EP_LD + i) * 4u;
@@ -411,8 +434,11 @@ __device__ void epilogue_cluster(const GemmParams& p, const Item& it, const floa
         v_up += part_up[r];
       }
     }
-    epi_store(p, it, m, i, v, v_up);
+    ep[m * EP_LD + i] = sw ? swiglu_clamped(v, v_up, p.clamp) : v;
   }
+  consumer_bar<NTHR>();
+  if (tid < ks) mbar_arrive_remote(mapa_shared(smem_u32(red_done), tid));  // one lane per peer
+  store_rows<EP_LD, NTHR>(p, it, ep, m_lo, per, tid);
 }
 
 // E8M0 byte -> 2^(e-127) for e in 1..254 by placing the byte in the f32 exponent field
@@ -423,14 +449,15 @@ __device__ __forceinline__ float e8m0_fast(uint32_t word, int byte) {
 }
 
 // ------------------------------------------------------------------------------ consumer
-template <int FMT, int NT, int NSTAGE>
+template <int FMT, int NT, int NSTAGE, int KS>
 __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t* smem,
                               uint64_t* full, uint64_t* empty, uint64_t* red_full,
                               uint64_t* red_done, volatile int* abort) {
-  using L = GemmLayout<FMT, NT, NSTAGE>;
+  using L = GemmLayout<FMT, NT, NSTAGE, KS>;
   constexpr int ASTR = FmtTraits<FMT>::ACT_STRIDE;
   constexpr int NB = FmtTraits<FMT>::KC / 32;  // 32-wide K blocks per stage
-  constexpr int HB = NB / KSW;                 // blocks per K share
+  constexpr int CONSUMER_WARPS = 4 * KS, NTHR = CONSUMER_WARPS * 32;
+  constexpr int HB = NB / KS;                  // blocks per K share
   const int tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31;
   const int mt = w & 3, kh = w >> 2;           // M-tile and K-half of this warp
@@ -463,7 +490,7 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
       const uint8_t* wr1 = wr0 + 8 * BOX_BYTES;
       const uint8_t* sc = smem + L::SC_OFF + s * L::SC_BYTES;
       const uint8_t* act = smem + L::ACT_OFF + s * L::ACT_BYTES + g * ASTR;
-      if (FMT == 4) {
+      if constexpr (FMT == 4) {
         uint32_t sa[HB / 4], sb[HB / 4];
 #pragma unroll
         for (int j = 0; j < HB / 4; ++j) {
@@ -519,17 +546,37 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
           e4m3x4_to_f16x4(wb1[j], hb1);
           const uint32_t A0[4] = {ha0[0], hb0[0], ha0[1], hb0[1]};
           const uint32_t A1[4] = {ha1[0], hb1[0], ha1[1], hb1[1]};
-          const float sf = e8m0_fast(sc4, b);
+          const uint32_t e = __byte_perm(sc4, 0u, 0x4440u + b);  // the same for the whole warp
+          if (NT >= 4 && e - 112u <= 22u) {
+            // scale 2^-15 .. 2^7: the scaled weights are exact in f16, so the MMAs accumulate
+            // every block straight into the tile accumulators
+            const uint32_t hs = e >= 113u ? (e - 112u) << 10 : 0x0200u;  // f16 2^(e-127)
+            const uint32_t s2 = hs | (hs << 16);
+            uint32_t A0s[4], A1s[4];
 #pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            if (NT == 1 || t < ntl) {
-              const uint2 b0 = lds64(act + t * 8 * ASTR + (32 * b + 4 * c) * 2);
-              const uint2 b1 = lds64(act + t * 8 * ASTR + (32 * b + 16 + 4 * c) * 2);
-              float d[4];
-              mma_f16(d, A0, b0.x, b0.y);
-              mma_f16_acc(d, A1, b1.x, b1.y);
+            for (int q = 0; q < 4; ++q) A0s[q] = hmul2(A0[q], s2), A1s[q] = hmul2(A1[q], s2);
 #pragma unroll
-              for (int jj = 0; jj < 4; ++jj) acc[t][jj] = fmaf(sf, d[jj], acc[t][jj]);
+            for (int t = 0; t < NT; ++t) {
+              if (t < ntl) {
+                const uint2 b0 = lds64(act + t * 8 * ASTR + (32 * b + 4 * c) * 2);
+                const uint2 b1 = lds64(act + t * 8 * ASTR + (32 * b + 16 + 4 * c) * 2);
+                mma_f16_acc(acc[t], A0s, b0.x, b0.y);
+                mma_f16_acc(acc[t], A1s, b1.x, b1.y);
+              }
+            }
+          } else {
+            const float sf = __uint_as_float(e << 23);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              if (NT == 1 || t < ntl) {
+                const uint2 b0 = lds64(act + t * 8 * ASTR + (32 * b + 4 * c) * 2);
+                const uint2 b1 = lds64(act + t * 8 * ASTR + (32 * b + 16 + 4 * c) * 2);
+                float d[4];
+                mma_f16(d, A0, b0.x, b0.y);
+                mma_f16_acc(d, A1, b1.x, b1.y);
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) acc[t][jj] = fmaf(sf, d[jj], acc[t][jj]);
+              }
             }
           }
         }
@@ -553,40 +600,39 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
       }
     }
     if (*abort) return;
-    if (KSW > 1) {  // the K shares' tiles, added in a fixed order
-      consumer_bar();
+    if (KS > 1) {  // the K shares' tiles, added in a fixed order
+      consumer_bar<NTHR>();
       const int cols = ntl * 8;
-      for (int idx = tid; idx < TILE_M * cols; idx += CONSUMER_WARPS * 32) {
+      for (int idx = tid; idx < TILE_M * cols; idx += NTHR) {
         const int m = idx / cols, col = idx - m * cols;
-        for (int k = 1; k < KSW; ++k) ep[m * L::EP_LD + col] += ep[k * TILE_M * L::EP_LD + m * L::EP_LD + col];
+        float v = ep[m * L::EP_LD + col];
+#pragma unroll
+        for (int k = 1; k < KS; ++k) v += ep[k * TILE_M * L::EP_LD + m * L::EP_LD + col];
+        ep[m * L::EP_LD + col] = v;
       }
     }
     if (clustered) {
       fence_acq_rel_cluster();
-      consumer_bar();
-      if (tid == 0)
-        for (int r = 0; r < p.ksplit; ++r) mbar_arrive_remote(mapa_shared(smem_u32(red_full), r));
+      consumer_bar<NTHR>();
+      if (tid < p.ksplit) mbar_arrive_remote(mapa_shared(smem_u32(red_full), tid));  // one lane per rank
       if (!pipe_wait<true>(red_full, tiles_done & 1, p.status, abort)) return;
-      epilogue_cluster<L::EP_LD>(p, it, ep, tid, rank, p.ksplit);
-      fence_acq_rel_cluster();
-      consumer_bar();
-      if (tid == 0)
-        for (int r = 0; r < p.ksplit; ++r) mbar_arrive_remote(mapa_shared(smem_u32(red_done), r));
+      epilogue_cluster<L::EP_LD, NTHR>(p, it, ep, tid, rank, p.ksplit, red_done);
     } else {
-      consumer_bar();
-      epilogue_local<L::EP_LD>(p, it, ep, tid);
-      consumer_bar();
+      consumer_bar<NTHR>();
+      epilogue_local<L::EP_LD, NTHR>(p, it, ep, tid);
     }
+    consumer_bar<NTHR>();  // the tile is written out before the next partial overwrites it
     ++tiles_done;
   }
   // no peer may still be reading this CTA's shared memory when it exits
   if (clustered && tiles_done > 0) pipe_wait<true>(red_done, (tiles_done - 1) & 1, p.status, abort);
 }
 
-template <int FMT, int NT, int NSTAGE>
-__global__ void __launch_bounds__(GEMM_THREADS)
+template <int FMT, int NT, int NSTAGE, int KS>
+__global__ void __launch_bounds__(gemm_threads(KS), FMT == 4 ? 3 : 2)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap map, const GemmParams p) {
-  using L = GemmLayout<FMT, NT, NSTAGE>;
+  using L = GemmLayout<FMT, NT, NSTAGE, KS>;
+  constexpr int CONSUMER_WARPS = 4 * KS, THREADS = gemm_threads(KS);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -616,30 +662,30 @@ __global__ void __launch_bounds__(GEMM_THREADS)
   pdl_trigger();
   // weights do not depend on the previous kernel: start streaming them before waiting on it
   int pre = 0;
-  if (warp == CONSUMER_WARPS) pre = prefetch_weights<FMT, NT, NSTAGE>(p, &map, smem, full);
+  if (warp == CONSUMER_WARPS) pre = prefetch_weights<FMT, NT, NSTAGE, KS>(p, &map, smem, full);
   pdl_wait();
   RouteSmem* rs = nullptr;
   if constexpr (L::EXPERT) {
     if (p.route) {
       rs = reinterpret_cast<RouteSmem*>(smem + L::ROUTE_OFF);
       const int nh = min(p.route->n_hit, MAX_EXPERTS);
-      for (int i = threadIdx.x; i < nh; i += GEMM_THREADS) {
+      for (int i = threadIdx.x; i < nh; i += THREADS) {
         rs->hit_e[i] = p.route->hit_e[i];
         rs->hit_off[i] = p.route->hit_off[i];
         rs->hit_cnt[i] = p.route->hit_cnt[i];
       }
-      for (int i = threadIdx.x; i <= nh; i += GEMM_THREADS) rs->rg_prefix[i] = p.route->rg_prefix[i];
+      for (int i = threadIdx.x; i <= nh; i += THREADS) rs->rg_prefix[i] = p.route->rg_prefix[i];
       if (p.act_rowmap)
-        for (int i = threadIdx.x; i < min(p.n_slots, MAX_SLOTS); i += GEMM_THREADS)
+        for (int i = threadIdx.x; i < min(p.n_slots, MAX_SLOTS); i += THREADS)
           rs->rowmap[i] = p.act_rowmap[i];
       if (threadIdx.x == 0) rs->n_hit = nh;
       __syncthreads();
     }
   }
   if (warp == CONSUMER_WARPS)
-    gemm_producer<FMT, NT, NSTAGE>(p, rs, &map, smem, full, empty, abort, pre);
+    gemm_producer<FMT, NT, NSTAGE, KS>(p, rs, &map, smem, full, empty, abort, pre);
   else
-    gemm_consumer<FMT, NT, NSTAGE>(p, rs, smem, full, empty, red_full, red_done, abort);
+    gemm_consumer<FMT, NT, NSTAGE, KS>(p, rs, smem, full, empty, red_full, red_done, abort);
 }
 
 }  // namespace mono
