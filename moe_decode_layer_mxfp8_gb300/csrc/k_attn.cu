@@ -69,15 +69,18 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(AttnArgs a) {
   float* sc = reinterpret_cast<float*>(sm + L::S_OFF);     // [16][SS] scores
   float* ks = reinterpret_cast<float*>(sm + L::SC_OFF);    // [128] per-key scales
   __shared__ float s_m[ATTN_HEADS], s_l[ATTN_HEADS], red[32];
+  __shared__ const uint8_t* s_rec[ATTN_KEYS];
   __shared__ int s_flag;
   pdl_trigger();
-  pdl_wait();
+  // Everything up to griddepcontrol.wait reads only the step's inputs (positions, requests,
+  // page table), none of which a kernel of the layer writes.
   const int r = blockIdx.x, g = blockIdx.y, sp = blockIdx.z, S = a.splits;
   const int G = a.kv_dim / DH, hpg = a.n_q / G, h0 = g * hpg;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int QW = a.n_q * DH;
   const int p = a.positions[r];
   if (p < 0) {  // pad row: attention output is zero
+    pdl_wait();
     if (sp == 0)
       for (int i = tid; i < hpg * DH; i += ATTN_THREADS)
         a.o[(size_t)r * QW + h0 * DH + i] = __float2half(0.0f);
@@ -95,6 +98,22 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(AttnArgs a) {
   const int t0 = lo + sp * per;
   const int nt = max(0, min(per, hi + 1 - t0));
   const int ntp = (nt + 15) & ~15;  // keys padded to whole MMA k-steps
+  // the split's KV records (null: padding or an unmapped page)
+  for (int t = tid; t < ntp; t += ATTN_THREADS) {
+    const uint8_t* rec = nullptr;
+    if (t < nt) {
+      const int pos = t0 + t;
+      const int pb = page_of(a.block_table, a.max_blocks, a.n_req, a.num_blocks, req, pos,
+                             a.block_size);
+      if (pb >= 0)
+        rec = a.cache + (size_t)pb * a.stride_block + (size_t)(pos % a.block_size) * a.stride_tok;
+      else
+        atomicOr(a.status, ST_UNMAPPED_PAGE);
+    }
+    s_rec[t] = rec;
+  }
+  __syncthreads();
+  pdl_wait();
 
   // q of the slice's heads (rows >= hpg zero), keys' codes and scales of the split
   constexpr int QC = DH / 8;  // 8-element chunks per head
@@ -110,33 +129,34 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(AttnArgs a) {
     *reinterpret_cast<uint4*>(qs + h * L::QS + c * 8) = o;
   }
   constexpr int KC = DH / 16;  // 16-byte code chunks per key
-  float smax = 0.0f;
-  for (int idx = tid; idx < ntp * KC; idx += ATTN_THREADS) {
+  constexpr int NL = ATTN_KEYS * KC / ATTN_THREADS;  // chunks per thread at most
+  uint4 raw[NL];
+  float scl[NL];
+#pragma unroll
+  for (int u = 0; u < NL; ++u) {  // every load in flight before the first use
+    const int idx = tid + u * ATTN_THREADS;
     const int t = idx / KC, c = idx - t * KC;
-    uint4 lo16 = {0u, 0u, 0u, 0u}, hi16 = {0u, 0u, 0u, 0u};
-    float s = 0.0f;
-    if (t < nt) {
-      const int pos = t0 + t;
-      const int pb = page_of(a.block_table, a.max_blocks, a.n_req, a.num_blocks, req, pos,
-                             a.block_size);
-      if (pb >= 0) {
-        const uint8_t* rec =
-            a.cache + (size_t)pb * a.stride_block + (size_t)(pos % a.block_size) * a.stride_tok;
-        const uint4 raw = *reinterpret_cast<const uint4*>(rec + g * DH + c * 16);
-        s = *reinterpret_cast<const float*>(rec + a.kv_dim);
-        uint32_t h2[2];
-        e4m3x4_to_f16x4(raw.x, h2); lo16.x = h2[0]; lo16.y = h2[1];
-        e4m3x4_to_f16x4(raw.y, h2); lo16.z = h2[0]; lo16.w = h2[1];
-        e4m3x4_to_f16x4(raw.z, h2); hi16.x = h2[0]; hi16.y = h2[1];
-        e4m3x4_to_f16x4(raw.w, h2); hi16.z = h2[0]; hi16.w = h2[1];
-      } else if (c == 0) {
-        atomicOr(a.status, ST_UNMAPPED_PAGE);
-      }
+    const uint8_t* rec = t < ntp ? s_rec[t] : nullptr;
+    raw[u] = rec ? *reinterpret_cast<const uint4*>(rec + g * DH + c * 16) : make_uint4(0u, 0u, 0u, 0u);
+    scl[u] = rec ? *reinterpret_cast<const float*>(rec + a.kv_dim) : 0.0f;
+  }
+  float smax = 0.0f;
+#pragma unroll
+  for (int u = 0; u < NL; ++u) {
+    const int idx = tid + u * ATTN_THREADS;
+    const int t = idx / KC, c = idx - t * KC;
+    if (t < ntp) {
+      uint4 lo16, hi16;
+      uint32_t h2[2];
+      e4m3x4_to_f16x4(raw[u].x, h2); lo16.x = h2[0]; lo16.y = h2[1];
+      e4m3x4_to_f16x4(raw[u].y, h2); lo16.z = h2[0]; lo16.w = h2[1];
+      e4m3x4_to_f16x4(raw[u].z, h2); hi16.x = h2[0]; hi16.y = h2[1];
+      e4m3x4_to_f16x4(raw[u].w, h2); hi16.z = h2[0]; hi16.w = h2[1];
+      *reinterpret_cast<uint4*>(kc + t * L::QS + c * 16) = lo16;
+      *reinterpret_cast<uint4*>(kc + t * L::QS + c * 16 + 8) = hi16;
+      if (c == 0) ks[t] = scl[u];
+      smax = fmaxf(smax, scl[u]);
     }
-    *reinterpret_cast<uint4*>(kc + t * L::QS + c * 16) = lo16;
-    *reinterpret_cast<uint4*>(kc + t * L::QS + c * 16 + 8) = hi16;
-    if (c == 0) ks[t] = s;
-    smax = fmaxf(smax, s);
   }
   smax = block_max(smax, red);  // (its barriers also publish q, codes and scales)
   const float inv_smax = smax > 0.0f ? 1.0f / smax : 0.0f;
@@ -177,7 +197,7 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(AttnArgs a) {
   }
   __syncthreads();
   // o = P' . codes: warps take 8-dim tiles
-  const int PW = DH + 2;
+  const int PW = DH + ATTN_PART_HEAD;
   for (int dt = warp; dt < DH / 8; dt += ATTN_THREADS / 32) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int kk = 0; kk < ntp / 16; ++kk) {
@@ -198,8 +218,7 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(AttnArgs a) {
             pack_f16x2(round_bf16(v0 * il), round_bf16(v1 * il));
       } else {
         float* part = a.part + (((size_t)r * a.n_q + h0 + h) * S + sp) * PW;
-        part[2 + d] = v0;
-        part[3 + d] = v1;
+        *reinterpret_cast<float2*>(part + ATTN_PART_HEAD + d) = make_float2(v0, v1);
         if (d == 0) part[0] = s_m[h], part[1] = s_l[h];
       }
     }
@@ -212,35 +231,40 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(AttnArgs a) {
   __syncthreads();
   if (!s_flag) return;
   __threadfence();
-  for (int idx = tid; idx < hpg * (DH / 2); idx += ATTN_THREADS) {
-    const int h = idx / (DH / 2), d = 2 * (idx - h * (DH / 2));
+  // a thread per (head, 4 dims); every split's values are in flight at once
+  for (int idx = tid; idx < hpg * (DH / 4); idx += ATTN_THREADS) {
+    const int h = idx / (DH / 4), d = 4 * (idx - h * (DH / 4));
     const float* base = a.part + ((size_t)r * a.n_q + h0 + h) * S * PW;
-    float ms[ATTN_MAX_SPLITS], ls[ATTN_MAX_SPLITS], o0[ATTN_MAX_SPLITS], o1[ATTN_MAX_SPLITS];
+    float ms[ATTN_MAX_SPLITS], ls[ATTN_MAX_SPLITS];
+    float4 os[ATTN_MAX_SPLITS];
 #pragma unroll
     for (int s = 0; s < ATTN_MAX_SPLITS; ++s) {
       if (s < S) {
-        ms[s] = __ldcg(base + s * PW);
-        ls[s] = __ldcg(base + s * PW + 1);
-        o0[s] = __ldcg(base + s * PW + 2 + d);
-        o1[s] = __ldcg(base + s * PW + 3 + d);
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(base + s * PW));
+        ms[s] = ml.x;
+        ls[s] = ml.y;
+        os[s] = __ldcg(reinterpret_cast<const float4*>(base + s * PW + ATTN_PART_HEAD + d));
       }
     }
     float M = -INFINITY;
 #pragma unroll
     for (int s = 0; s < ATTN_MAX_SPLITS; ++s)
       if (s < S) M = fmaxf(M, ms[s]);
-    float n0 = 0.0f, n1 = 0.0f, den = 0.0f;
+    float n0 = 0.0f, n1 = 0.0f, n2 = 0.0f, n3 = 0.0f, den = 0.0f;
 #pragma unroll
     for (int s = 0; s < ATTN_MAX_SPLITS; ++s) {
       if (s < S) {
         const float f = ms[s] == -INFINITY ? 0.0f : expf(ms[s] - M);
-        n0 = fmaf(f, o0[s], n0);
-        n1 = fmaf(f, o1[s], n1);
+        n0 = fmaf(f, os[s].x, n0);
+        n1 = fmaf(f, os[s].y, n1);
+        n2 = fmaf(f, os[s].z, n2);
+        n3 = fmaf(f, os[s].w, n3);
         den = fmaf(f, ls[s], den);
       }
     }
-    *reinterpret_cast<uint32_t*>(a.o + (size_t)r * QW + (h0 + h) * DH + d) =
-        pack_f16x2(round_bf16(n0 / den), round_bf16(n1 / den));
+    *reinterpret_cast<uint2*>(a.o + (size_t)r * QW + (h0 + h) * DH + d) =
+        make_uint2(pack_f16x2(round_bf16(n0 / den), round_bf16(n1 / den)),
+                   pack_f16x2(round_bf16(n2 / den), round_bf16(n3 / den)));
   }
   if (tid == 0) *ctr = 0;
 }

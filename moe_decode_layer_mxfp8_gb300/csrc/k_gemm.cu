@@ -12,7 +12,7 @@ struct Var;
 template <> struct Var<8, 1> { static constexpr int NSTAGE = 6, KS = 2; };
 template <> struct Var<8, 2> { static constexpr int NSTAGE = 6, KS = 2; };
 template <> struct Var<8, 4> { static constexpr int NSTAGE = 4, KS = 2; };
-template <> struct Var<8, 6> { static constexpr int NSTAGE = 4, KS = 2; };
+template <> struct Var<8, 6> { static constexpr int NSTAGE = 3, KS = 2; };
 template <> struct Var<4, 1> { static constexpr int NSTAGE = 4, KS = 1; };
 
 template <int FMT, int NT>

@@ -19,17 +19,19 @@ constexpr int NORM_CHUNKS = 4;  // 8-element chunks per thread: rows up to 8192 
 __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(NormArgs a) {
   __shared__ float red[32];
   pdl_trigger();
-  pdl_wait();
   const int r = blockIdx.x, tid = threadIdx.x;
   const __nv_bfloat16* x = a.in + (size_t)r * a.in_ld;
   uint4 xv[NORM_CHUNKS], gv[NORM_CHUNKS];
 #pragma unroll
+  for (int c = 0; c < NORM_CHUNKS; ++c) {  // gamma is constant: fetched before the wait
+    const int i = (c * NORM_THREADS + tid) * 8;
+    if (i < a.dim) gv[c] = *reinterpret_cast<const uint4*>(a.gamma + i);
+  }
+  pdl_wait();
+#pragma unroll
   for (int c = 0; c < NORM_CHUNKS; ++c) {
     const int i = (c * NORM_THREADS + tid) * 8;
-    if (i < a.dim) {
-      xv[c] = *reinterpret_cast<const uint4*>(x + i);
-      gv[c] = *reinterpret_cast<const uint4*>(a.gamma + i);
-    }
+    if (i < a.dim) xv[c] = *reinterpret_cast<const uint4*>(x + i);
   }
   float ss = 0.0f;
 #pragma unroll
@@ -78,26 +80,27 @@ constexpr int QKV_CHUNKS = 2;  // q latents up to 4096 wide
 __global__ void __launch_bounds__(NORM_THREADS) qkv_norm_insert_kernel(QkvNormInsertArgs a) {
   __shared__ float red[32];
   pdl_trigger();
-  pdl_wait();
   const int r = blockIdx.x, tid = threadIdx.x;
   const __nv_bfloat16* row = a.qkv + (size_t)r * (a.q_rank + a.kv_dim);
   const bool has_kv = tid * 8 < a.kv_dim;  // kv_dim <= 1024: one chunk per thread at most
   uint4 qv[QKV_CHUNKS], qg[QKV_CHUNKS], kv = {}, kg = {};
+  // the gammas and the step's inputs (position, page table) before the wait
 #pragma unroll
   for (int c = 0; c < QKV_CHUNKS; ++c) {
     const int i = (c * NORM_THREADS + tid) * 8;
-    if (i < a.q_rank) {
-      qv[c] = *reinterpret_cast<const uint4*>(row + i);
-      qg[c] = *reinterpret_cast<const uint4*>(a.gq + i);
-    }
+    if (i < a.q_rank) qg[c] = *reinterpret_cast<const uint4*>(a.gq + i);
   }
-  if (has_kv) {
-    kv = *reinterpret_cast<const uint4*>(row + a.q_rank + tid * 8);
-    kg = *reinterpret_cast<const uint4*>(a.gkv + tid * 8);
-  }
+  if (has_kv) kg = *reinterpret_cast<const uint4*>(a.gkv + tid * 8);
   const int p = a.positions[r];
   const int pb = p < 0 ? -1 : page_of(a.block_table, a.max_blocks, a.n_req, a.num_blocks,
                                      a.row_req[r], p, a.block_size);
+  pdl_wait();
+#pragma unroll
+  for (int c = 0; c < QKV_CHUNKS; ++c) {
+    const int i = (c * NORM_THREADS + tid) * 8;
+    if (i < a.q_rank) qv[c] = *reinterpret_cast<const uint4*>(row + i);
+  }
+  if (has_kv) kv = *reinterpret_cast<const uint4*>(row + a.q_rank + tid * 8);
   float ssq = 0.0f, sskv = 0.0f;
 #pragma unroll
   for (int c = 0; c < QKV_CHUNKS; ++c) {
@@ -176,12 +179,13 @@ constexpr int FINAL_COLS = FINAL_THREADS * 8;
 constexpr int FINAL_MAX_K = 8;
 __global__ void __launch_bounds__(FINAL_THREADS) final_kernel(FinalArgs a) {
   pdl_trigger();
-  pdl_wait();
   const int r = blockIdx.x;
   const int c = blockIdx.y * FINAL_COLS + threadIdx.x * 8;
+  const bool pad = a.positions[r] < 0;  // a step input: read before the wait
+  pdl_wait();
   if (c >= a.H) return;
   const size_t o = (size_t)r * a.H + c;
-  if (a.positions[r] < 0) {
+  if (pad) {
     *reinterpret_cast<uint4*>(a.out + o) = *reinterpret_cast<const uint4*>(a.x + o);
     return;
   }

@@ -2,10 +2,17 @@
 // table K2: "router, top-6"; ATOM changes: "f32 router logits").
 //
 // router_kernel: z[r, e] = u[r] . W_r[e] in f32, split over K: CTA (4 experts, 1024-wide K
-// slice) stages the slice of every row of u in shared memory and writes one partial per
-// (slice, row, expert).  topk_kernel sums the partials in slice order (a fixed order, so
-// results replay bit-exactly), picks the top-k per row and sorts the (row, slot) pairs by
-// expert, stably, for the grouped expert GEMMs.
+// slice) holds its experts' weight slices in registers (fetched before waiting on the
+// previous kernel), reads the slice of every row of u and writes one partial per (slice,
+// row, expert).  Rows go two at a time: two independent FMA chains per lane, then one
+// transposing butterfly that leaves each half-warp with one row's sum.
+//
+// topk_kernel sums the partials in slice order (a fixed order, so results replay
+// bit-exactly) into shared memory, picks the top-k per row (a warp per row: the largest key
+// by warp max-reduction, ties to the lowest expert index by a min-reduction) and sorts the
+// (row, slot) pairs by expert, stably, for the grouped expert GEMMs: a row picks an expert
+// at most once, so an entry's place among its expert's entries is the number of earlier
+// rows in that expert's row mask.
 #include "kernels.h"
 
 namespace mono {
@@ -14,111 +21,142 @@ namespace {
 
 constexpr int RT_EXPERTS = 4;    // experts per CTA, one warp each
 constexpr int RT_THREADS = RT_EXPERTS * 32;
+constexpr int RT_J = ROUTER_KSLICE / 128;  // float4 weight chunks per lane
 constexpr int MAX_ROWS = 48, MAX_K = 8;
 
-__global__ void __launch_bounds__(RT_THREADS) router_kernel(RouterArgs a) {
-  extern __shared__ __align__(16) uint8_t rt_smem[];
-  __half* us = reinterpret_cast<__half*>(rt_smem);  // [rows][ROUTER_KSLICE]
+__global__ void __launch_bounds__(RT_THREADS, 8) router_kernel(RouterArgs a) {
   pdl_trigger();
-  pdl_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int k0 = blockIdx.y * ROUTER_KSLICE;
   const int klen = min(ROUTER_KSLICE, a.H - k0);
-  const int chunks = klen / 8;  // 16-byte chunks per row
-  for (int idx = tid; idx < a.rows * chunks; idx += RT_THREADS) {
-    const int r = idx / chunks, c = idx - r * chunks;
-    cp_async16(us + r * ROUTER_KSLICE + c * 8, a.u + (size_t)r * a.H + k0 + c * 8, 16);
-  }
-  asm volatile("cp.async.wait_all;" ::: "memory");
-  // this lane's weights: k = k0 + 128 j + 4 lane + {0..3}
+  // this lane's weights (k = k0 + 128 j + 4 lane + {0..3}): constant, so fetched first
   const int e = blockIdx.x * RT_EXPERTS + warp;
-  float4 wv[ROUTER_KSLICE / 128];
-  if (e < a.E) {
-    const float* wr = a.wr + (size_t)e * a.H + k0;
+  float4 wv[RT_J];
 #pragma unroll
-    for (int j = 0; j < ROUTER_KSLICE / 128; ++j)
-      wv[j] = 128 * j < klen ? *reinterpret_cast<const float4*>(wr + 128 * j + 4 * lane)
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  __syncthreads();
+  for (int j = 0; j < RT_J; ++j)
+    wv[j] = e < a.E && 128 * j < klen
+                ? *reinterpret_cast<const float4*>(a.wr + (size_t)e * a.H + k0 + 128 * j + 4 * lane)
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+  pdl_wait();
   if (e >= a.E) return;
-  for (int r = 0; r < a.rows; ++r) {
-    const __half* ur = us + r * ROUTER_KSLICE + 4 * lane;
-    float acc = 0.0f;
+  // u is read straight from L2 through L1 (the CTA's four warps read the same values), so
+  // the kernel needs no shared memory and, at 64 registers or fewer, fits beside the shared
+  // expert's GEMM CTAs.  Lane l ends a pair of rows with the sum of row bit4(l).
+  for (int r0 = 0; r0 < a.rows; r0 += 2) {
+    uint2 uv[2][RT_J];
 #pragma unroll
-    for (int j = 0; j < ROUTER_KSLICE / 128; ++j) {
-      if (128 * j < klen) {
-        const uint2 uv = lds64(ur + 128 * j);
-        const float2 u0 = __half22float2(*reinterpret_cast<const __half2*>(&uv.x));
-        const float2 u1 = __half22float2(*reinterpret_cast<const __half2*>(&uv.y));
-        acc = fmaf(u0.x, wv[j].x, acc);
-        acc = fmaf(u0.y, wv[j].y, acc);
-        acc = fmaf(u1.x, wv[j].z, acc);
-        acc = fmaf(u1.y, wv[j].w, acc);
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int j = 0; j < RT_J; ++j)
+        uv[i][j] = r0 + i < a.rows && 128 * j < klen
+                       ? __ldg(reinterpret_cast<const uint2*>(a.u + (size_t)(r0 + i) * a.H + k0 +
+                                                              128 * j + 4 * lane))
+                       : make_uint2(0u, 0u);
+    float acc[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      acc[i] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < RT_J; ++j) {
+        const float2 u0 = __half22float2(*reinterpret_cast<const __half2*>(&uv[i][j].x));
+        const float2 u1 = __half22float2(*reinterpret_cast<const __half2*>(&uv[i][j].y));
+        acc[i] = fmaf(u0.x, wv[j].x, acc[i]);
+        acc[i] = fmaf(u0.y, wv[j].y, acc[i]);
+        acc[i] = fmaf(u1.x, wv[j].z, acc[i]);
+        acc[i] = fmaf(u1.y, wv[j].w, acc[i]);
       }
     }
-    acc = warp_sum(acc);
-    if (lane == 0) a.partial[((size_t)blockIdx.y * a.rows + r) * a.E + e] = acc;
+    // transposing butterfly: 2 values over 32 lanes -> 1 row sum per lane (5 shuffles)
+    const bool b4 = lane & 16;
+    float v = (b4 ? acc[1] : acc[0]) + __shfl_xor_sync(0xffffffffu, b4 ? acc[0] : acc[1], 16);
+    v += __shfl_xor_sync(0xffffffffu, v, 8);
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    const int my_row = r0 + (b4 ? 1 : 0);
+    if ((lane & 15) == 0 && my_row < a.rows)
+      a.partial[((size_t)blockIdx.y * a.rows + my_row) * a.E + e] = v;
   }
+}
+
+// f32 -> unsigned key with the same order (larger float, larger key)
+__device__ __forceinline__ uint32_t order_key(float z) {
+  const uint32_t u = __float_as_uint(z);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 constexpr int TOPK_THREADS = 512;
 __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
+  extern __shared__ float s_z[];  // [rows][E] logits
   __shared__ int s_idx[MAX_ROWS * MAX_K];
-  __shared__ int s_cnt[MAX_EXPERTS], s_off[MAX_EXPERTS], s_hit[MAX_EXPERTS], s_rg[MAX_EXPERTS];
-  __shared__ int s_fill[MAX_EXPERTS];
+  __shared__ unsigned long long s_mask[MAX_EXPERTS];  // rows routed to each expert
+  __shared__ int s_off[MAX_EXPERTS];
   pdl_trigger();
-  pdl_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int NW = TOPK_THREADS / 32, ZJ = MAX_EXPERTS / 32;
-  for (int e = tid; e < MAX_EXPERTS; e += TOPK_THREADS) s_cnt[e] = 0, s_fill[e] = 0;
-  // phase 1: logits (sum of the K-slice partials in slice order) and selection, a warp a row
-  for (int r = warp; r < a.rows; r += NW) {
-    const bool pad = a.positions[r] < 0;
-    float z[ZJ];
+  for (int e = tid; e < MAX_EXPERTS; e += TOPK_THREADS) s_mask[e] = 0ull;
+  pdl_wait();
+  // phase 1a: logits = the K-slice partials summed in slice order, every load of a batch of
+  // four logits in flight at once
+  const int nz = a.rows * a.E;
+  for (int base = tid; base < nz; base += 4 * TOPK_THREADS) {
+    float pz[4][ROUTER_MAX_KSLICES];
 #pragma unroll
-    for (int j = 0; j < ZJ; ++j) z[j] = 0.0f;
-    for (int ks = 0; ks < a.kslices; ++ks) {
-      float pz[ZJ];
+    for (int u = 0; u < 4; ++u)
 #pragma unroll
-      for (int j = 0; j < ZJ; ++j) {
-        const int e = lane + 32 * j;
-        pz[j] = e < a.E ? a.partial[((size_t)ks * a.rows + r) * a.E + e] : 0.0f;
+      for (int ks = 0; ks < ROUTER_MAX_KSLICES; ++ks) {
+        const int i = base + u * TOPK_THREADS;
+        pz[u][ks] = i < nz && ks < a.kslices ? a.partial[(size_t)ks * nz + i] : 0.0f;
       }
 #pragma unroll
-      for (int j = 0; j < ZJ; ++j) z[j] += pz[j];
+    for (int u = 0; u < 4; ++u) {
+      const int i = base + u * TOPK_THREADS;
+      float z = 0.0f;
+#pragma unroll
+      for (int ks = 0; ks < ROUTER_MAX_KSLICES; ++ks)
+        if (ks < a.kslices) z += pz[u][ks];
+      if (i < nz) {
+        s_z[i] = z;
+        a.logits[i] = z;
+      }
     }
+  }
+  __syncthreads();
+  // phase 1b: selection, a warp a row
+  for (int r = warp; r < a.rows; r += NW) {
+    const bool pad = a.positions[r] < 0;
+    uint32_t key[ZJ];
 #pragma unroll
     for (int j = 0; j < ZJ; ++j) {
       const int e = lane + 32 * j;
-      if (e < a.E) a.logits[(size_t)r * a.E + e] = z[j];
-      else z[j] = -INFINITY;
+      key[j] = e < a.E ? order_key(s_z[r * a.E + e] + 0.0f) : 0u;  // (-0 -> +0); 0: below all
     }
+    // k rounds of: largest key over the warp, then the lowest expert index holding it
     float zsel0 = 0.0f, ex_sum = 0.0f, my_ex = 0.0f;
     int my_e = -1;
 #pragma unroll
     for (int kk = 0; kk < MAX_K; ++kk) {
       if (kk < a.k) {
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
+        uint32_t lk = 0u;
 #pragma unroll
-        for (int j = 0; j < ZJ; ++j) {
-          const int e = lane + 32 * j;
-          if (e < a.E && (z[j] > bv || (z[j] == bv && e < be))) bv = z[j], be = e;
-        }
+        for (int j = 0; j < ZJ; ++j) lk = max(lk, key[j]);
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, lk);
+        uint32_t cand = 0xffffffffu;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-          const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-          if (ov > bv || (ov == bv && oe < be)) bv = ov, be = oe;
-        }
+        for (int j = ZJ - 1; j >= 0; --j)
+          if (key[j] == mk) cand = lane + 32 * j;
+        const int be = (int)__reduce_min_sync(0xffffffffu, cand);
+        const float bv = key_value(mk);
         if (kk == 0) zsel0 = bv;
         const float ex = expf(bv - zsel0);
         ex_sum += ex;
         if (lane == kk) my_ex = ex, my_e = be;  // lane kk keeps slot kk
 #pragma unroll
         for (int j = 0; j < ZJ; ++j)
-          if (lane + 32 * j == be) z[j] = -INFINITY;
+          if (lane + 32 * j == be) key[j] = 0u;
       }
     }
     if (lane < a.k) {
@@ -129,19 +167,16 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
       a.topk_w[r * a.k + lane] = wgt;
       if (a.user_idx) a.user_idx[r * a.k + lane] = e;
       if (a.user_w) a.user_w[r * a.k + lane] = wgt;
+      if (e >= 0) atomicOr(&s_mask[e], 1ull << r);
     }
   }
-  __syncthreads();
-  const int n = a.rows * a.k;
-  for (int q = tid; q < n; q += TOPK_THREADS)
-    if (s_idx[q] >= 0) atomicAdd(&s_cnt[s_idx[q]], 1);
   __syncthreads();
   // phase 2: prefix sums over experts (one warp; E <= 256)
   if (warp == 0) {
     int run_off = 0, run_hit = 0, run_rg = 0;
     for (int base = 0; base < MAX_EXPERTS; base += 32) {
       const int e = base + lane;
-      const int c = e < a.E ? s_cnt[e] : 0;
+      const int c = e < a.E ? __popcll(s_mask[e]) : 0;
       const int hit = c > 0, rg = (c + EXPERT_ROWS - 1) / EXPERT_ROWS;
       int ic = c, ih = hit, ir = rg;
 #pragma unroll
@@ -152,8 +187,13 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
         if (lane >= o) ic += tc, ih += th, ir += tr;
       }
       s_off[e] = run_off + ic - c;
-      s_hit[e] = run_hit + ih - hit;
-      s_rg[e] = run_rg + ir - rg;
+      if (c > 0) {
+        const int d = run_hit + ih - hit;
+        a.route->hit_e[d] = e;
+        a.route->hit_off[d] = run_off + ic - c;
+        a.route->hit_cnt[d] = c;
+        a.route->rg_prefix[d] = run_rg + ir - rg;
+      }
       run_off += __shfl_sync(0xffffffffu, ic, 31);
       run_hit += __shfl_sync(0xffffffffu, ih, 31);
       run_rg += __shfl_sync(0xffffffffu, ir, 31);
@@ -164,57 +204,40 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
     }
   }
   __syncthreads();
-  for (int e = tid; e < a.E; e += TOPK_THREADS) {
-    if (s_cnt[e] > 0) {
-      const int d = s_hit[e];
-      a.route->hit_e[d] = e;
-      a.route->hit_off[d] = s_off[e];
-      a.route->hit_cnt[d] = s_cnt[e];
-      a.route->rg_prefix[d] = s_rg[e];
-    }
-  }
-  // phase 3: stable placement in (row, slot) order within each expert, 32 entries at a time
-  if (warp == 0) {
-    for (int base = 0; base < n; base += 32) {
-      const int q = base + lane;
-      const int e = q < n ? s_idx[q] : -1;
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
-      const int before = __popc(peers & ((1u << lane) - 1u));
-      const int fill = e >= 0 ? s_fill[e] : 0;
-      __syncwarp();
-      if (q < n) {
-        if (e >= 0) {
-          const int pos = s_off[e] + fill + before;
-          a.slot_pos[q] = pos;
-          a.perm[pos] = q / a.k;
-        } else {
-          a.slot_pos[q] = -1;
-        }
-      }
-      if (e >= 0 && before == 0) s_fill[e] = fill + __popc(peers);
-      __syncwarp();
+  // phase 3: stable placement -- an expert's entries in row order (a row picks an expert once)
+  const int n = a.rows * a.k;
+  for (int q = tid; q < n; q += TOPK_THREADS) {
+    const int e = s_idx[q];
+    if (e >= 0) {
+      const int r = q / a.k;
+      const int pos = s_off[e] + __popcll(s_mask[e] & ((1ull << r) - 1ull));
+      a.slot_pos[q] = pos;
+      a.perm[pos] = r;
+    } else {
+      a.slot_pos[q] = -1;
     }
   }
 }
 
 }  // namespace
 
-int router_smem_bytes(int rows) { return rows * ROUTER_KSLICE * 2; }
+// The logits of the step in shared memory, [rows][E].
+int topk_smem_bytes() { return MAX_ROWS * MAX_EXPERTS * 4; }
 
 // The limit is a property of the kernel, shared by every layer handle of the process: set it
 // for the largest step any handle accepts.
 cudaError_t router_prepare() {
-  return cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              router_smem_bytes(MAX_ROWS));
+  return cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              topk_smem_bytes());
 }
 
 cudaError_t launch_router(const Launch& L, const RouterArgs& a) {
   const dim3 grid((a.E + RT_EXPERTS - 1) / RT_EXPERTS, (a.H + ROUTER_KSLICE - 1) / ROUTER_KSLICE);
-  return launch_ex(L, grid, dim3(RT_THREADS), router_smem_bytes(a.rows), router_kernel, a);
+  return launch_ex(L, grid, dim3(RT_THREADS), 0, router_kernel, a);
 }
 
 cudaError_t launch_topk(const Launch& L, const TopkArgs& a) {
-  return launch_ex(L, dim3(1), dim3(TOPK_THREADS), 0, topk_kernel, a);
+  return launch_ex(L, dim3(1), dim3(TOPK_THREADS), a.rows * a.E * 4, topk_kernel, a);
 }
 
 }  // namespace mono

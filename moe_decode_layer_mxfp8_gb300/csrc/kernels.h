@@ -71,7 +71,9 @@ struct AttnArgs {
 };
 
 constexpr int ROUTER_KSLICE = 1024;  // K per router CTA (the router sums partial logits)
+constexpr int ROUTER_MAX_KSLICES = 8;  // hidden <= 8192
 constexpr int ATTN_MAX_SPLITS = 8;   // window splits of the attention at most
+constexpr int ATTN_PART_HEAD = 4;    // f32 words before a split's partial output: m, l, padding
 
 struct RouterArgs {
   const __half* u;  // [rows, H]

@@ -241,7 +241,7 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
     h->buf_off[b] = take(sizes[b]);
   }
   const size_t o_ctr = take((size_t)R * G * 4);
-  const size_t o_part = take((size_t)R * s.n_q_heads * attn_splits_max * (s.head_dim + 2) * 4);
+  const size_t o_part = take((size_t)R * s.n_q_heads * attn_splits_max * (s.head_dim + ATTN_PART_HEAD) * 4);
   const size_t o_status = take(16);
   const size_t o_route = take(sizeof(RouteInfo));
   const size_t o_perm = take((size_t)R * K * 4);
@@ -492,8 +492,9 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     t.stride_block = a->kv_stride_block;
     t.stride_tok = a->kv_stride_tok;
     t.num_blocks = a->kv_num_blocks;
-    const int want = (2 * h->num_sms + R * G - 1) / (R * G);
-    t.splits = std::max(h->attn_min_splits, std::min(ATTN_MAX_SPLITS, want));
+    // one split per 128 window keys: a single CTA reads a 128-key window faster than
+    // several CTAs read it and combine
+    t.splits = h->attn_min_splits;
     t.part = h->attn_part;
     t.counters = h->attn_counters;
     t.status = h->status;
@@ -507,8 +508,10 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
   // ---------------------------------------------------------------- K2: FFN seam and MoE
   RUN(launch_rmsnorm(L, {h->buf<__nv_bfloat16>(MONO_BUF_H), H, (const __nv_bfloat16*)h->w.ffn_norm,
                          H, s.eps, h->buf<__half>(MONO_BUF_U), H}, R));
-  // The shared expert depends only on u: fork it onto the side stream so that it overlaps
-  // the router and the top-k; the routed experts start once both branches are done.  While
+  RUN(launch_router(L, {h->buf<__half>(MONO_BUF_U), h->w.router, R, E, H, h->router_part}));
+  // The shared expert depends only on u: fork it onto the side stream after the router (whose
+  // CTAs are then resident before the shared expert's GEMM CTAs claim the SMs) so that it
+  // overlaps the top-k; the routed experts start once both branches are done.  While
   // profiling, everything stays on one stream in launch-name order.
   const bool fork = !h->profiling;
   const Launch Ls{fork ? h->side : stream, !h->profiling};
@@ -528,7 +531,6 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     if (rs != MONO_OK) return rs;
     RUN_PLAIN(cudaEventRecord(h->ev_join, h->side));
   }
-  RUN(launch_router(L, {h->buf<__half>(MONO_BUF_U), h->w.router, R, E, H, h->router_part}));
   {
     TopkArgs t = {};
     t.partial = h->router_part;

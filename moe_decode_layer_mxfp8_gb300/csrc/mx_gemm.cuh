@@ -112,7 +112,9 @@ struct GemmLayout {
   static constexpr int ACT_OFF = NSTAGE * W_STAGE_BYTES;
   static constexpr int SC_OFF = ACT_OFF + NSTAGE * ACT_BYTES;
   static constexpr int EP_OFF = align_up(SC_OFF + NSTAGE * SC_BYTES, 16);
-  static constexpr int EP_BYTES = KS * TILE_M * EP_LD * 4;  // one partial tile per K share
+  // one partial tile per K share, then (dense matrices) the K-split receive tile
+  static constexpr int EP_TILE = TILE_M * EP_LD;  // floats
+  static constexpr int EP_BYTES = (KS + (EXPERT ? 0 : 1)) * EP_TILE * 4;
   static constexpr int ROUTE_OFF = align_up(EP_OFF + EP_BYTES, 16);
   static constexpr int ROUTE_BYTES = EXPERT ? (int)sizeof(RouteSmem) : 0;
   static constexpr int BAR_OFF = align_up(ROUTE_OFF + ROUTE_BYTES, 16);
@@ -398,47 +400,120 @@ __device__ void epilogue_local(const GemmParams& p, const Item& it, float* ep, i
   store_rows<EP_LD, NTHR>(p, it, ep, 0, sw ? BOX_ROWS : TILE_M, tid);
 }
 
-// Epilogue of a K-split tile: this CTA (rank r of a cluster of ks) sums its slice of the
-// tile's rows over every CTA's partial, in rank order, through distributed shared memory,
-// and keeps the sums in its own partial's slice (rows no peer reads).  Once every consumer
-// thread has its sums, the CTA tells each peer that it is done reading the peer's partial,
-// then writes the slice out.
-template <int EP_LD, int NTHR>
-__device__ void epilogue_cluster(const GemmParams& p, const Item& it, float* ep, int tid,
-                                 uint32_t rank, int ks, uint64_t* red_done) {
-  const int n = it.n;
-  const bool sw = p.epi == EPI_SWIGLU_F16;
-  const int units = sw ? BOX_ROWS : TILE_M;
-  const int per = units / ks;
-  const int m_lo = (int)rank * per;
-  uint32_t peer[MAX_CLUSTER];
+// Accumulators of consumer warp (M-tile mt) into its K share's partial tile.
+template <int NT, int EP_LD>
+__device__ __forceinline__ void write_partial(const float (&acc)[NT][4], float* ep_mine, int mt,
+                                              int g, int c, int ntl) {
+  const int m0 = 16 * mt + g;
 #pragma unroll
-  for (int r = 0; r < MAX_CLUSTER; ++r) peer[r] = r < ks ? mapa_shared(smem_u32(ep), r) : 0u;
-  for (int idx = tid; idx < per * n; idx += NTHR) {
-    const int i = idx / per, m = m_lo + (idx - i * per);
-    const uint32_t off = (uint32_t)(m * EP_LD + i) * 4u;
-    const uint32_t off_up = (uint32_t)((m + BOX_ROWS) * EP_LD + i) * 4u;
-    float part[MAX_CLUSTER], part_up[MAX_CLUSTER];
-#pragma unroll
-    for (int r = 0; r < MAX_CLUSTER; ++r) {
-      if (r < ks) {
-        part[r] = ld_dsmem_f32(peer[r] + off);
-        part_up[r] = sw ? ld_dsmem_f32(peer[r] + off_up) : 0.0f;
-      }
+  for (int t = 0; t < NT; ++t) {
+    if (NT == 1 || t < ntl) {
+      const int col = t * 8 + 2 * c;
+      ep_mine[m0 * EP_LD + col] = acc[t][0];
+      ep_mine[m0 * EP_LD + col + 1] = acc[t][1];
+      ep_mine[(m0 + 8) * EP_LD + col] = acc[t][2];
+      ep_mine[(m0 + 8) * EP_LD + col + 1] = acc[t][3];
     }
-    float v = 0.0f, v_up = 0.0f;
-#pragma unroll
-    for (int r = 0; r < MAX_CLUSTER; ++r) {
-      if (r < ks) {
-        v += part[r];
-        v_up += part_up[r];
-      }
-    }
-    ep[m * EP_LD + i] = sw ? swiglu_clamped(v, v_up, p.clamp) : v;
   }
-  consumer_bar<NTHR>();
-  if (tid < ks) mbar_arrive_remote(mapa_shared(smem_u32(red_done), tid));  // one lane per peer
-  store_rows<EP_LD, NTHR>(p, it, ep, m_lo, per, tid);
+}
+
+// The K shares' partial tiles added, in a fixed order, into the first.
+template <int KS, int EP_LD, int NTHR>
+__device__ __forceinline__ void sum_kshares(float* ep, int ntl, int tid) {
+  const int cols = ntl * 8;
+  for (int idx = tid; idx < TILE_M * cols; idx += NTHR) {
+    const int m = idx / cols, col = idx - m * cols;
+    float v = ep[m * EP_LD + col];
+#pragma unroll
+    for (int k = 1; k < KS; ++k) v += ep[k * TILE_M * EP_LD + m * EP_LD + col];
+    ep[m * EP_LD + col] = v;
+  }
+}
+
+// K-split tiles across a cluster of ks CTAs.  Rank o owns weight rows (output columns)
+// [o * per, o * per + per) of the tile, per = 64 / ks -- for SwiGLU tiles per = 32 / ks gate
+// rows together with their up rows 32 further.  Each CTA pushes the owner's rows of its
+// partial tile into the owner's receive tile with bulk shared-to-shared copies that complete
+// on the owner's mbarrier, so the reduction costs one asynchronous transfer instead of
+// element-wise remote accesses; the owner adds the ks slots in rank order.  Receive tile:
+// slot s (source rank) holds 64 / ks rows of EP_LD floats (SwiGLU: gate rows, then up rows).
+template <int EP_LD>
+__device__ __forceinline__ void push_slices(const GemmParams& p, const float* part, float* recv,
+                                            uint64_t* red_full, uint32_t rank, int n) {
+  const bool sw = p.epi == EPI_SWIGLU_F16;
+  const int ks = p.ksplit;
+  const int per = (sw ? BOX_ROWS : TILE_M) / ks;
+  const uint32_t chunk = (uint32_t)(per * EP_LD * 4);  // bytes of one run of rows
+  const uint32_t srows = (uint32_t)(TILE_M / ks);
+  // this owner's slots arrive from every rank
+  mbar_arrive_expect_tx(red_full, (uint32_t)ks * srows * EP_LD * 4);
+  const uint32_t recv_u = smem_u32(recv), bar_u = smem_u32(red_full);
+  for (int o = 0; o < ks; ++o) {
+    const uint32_t dst = mapa_shared(recv_u + rank * srows * EP_LD * 4, (uint32_t)o);
+    const uint32_t bar = mapa_shared(bar_u, (uint32_t)o);
+    bulk_copy_s2s(dst, part + o * per * EP_LD, chunk, bar);
+    if (sw) bulk_copy_s2s(dst + chunk, part + (BOX_ROWS + o * per) * EP_LD, chunk, bar);
+  }
+  bulk_commit();
+  (void)n;
+}
+
+// The owner's share of a K-split tile: adds its receive slots in slot order and writes its
+// columns out, two values per thread in flight at a time.
+template <int EP_LD, int NTHR>
+__device__ void owner_epilogue(const GemmParams& p, const Item& it, const float* recv, int tid,
+                               uint32_t rank) {
+  const bool sw = p.epi == EPI_SWIGLU_F16;
+  const int ks = p.ksplit;
+  const int per = (sw ? BOX_ROWS : TILE_M) / ks;
+  const int srows = TILE_M / ks;
+  const int total = per * it.n;
+  const int ncols = sw ? p.swiglu_I : p.N;
+  constexpr int B = 2;
+  for (int base = tid; base < total; base += B * NTHR) {
+    float v[B], r[B];
+    size_t o[B];
+    bool ok[B];
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      const int idx = base + u * NTHR;
+      const int i = idx / per, lr = idx - (idx / per) * per;
+      const int col = it.col0 + (int)rank * per + lr;
+      ok[u] = idx < total && col < ncols;
+      o[u] = (size_t)(it.row0 + i) * p.out_ld + col;
+      r[u] = ok[u] && p.epi == EPI_RESID_BF16
+                 ? __bfloat162float(p.resid[(size_t)(it.row0 + i) * p.resid_ld + col])
+                 : 0.0f;
+      float s = 0.0f, su = 0.0f;
+      if (idx < total) {
+        for (int sl = 0; sl < ks; ++sl) {
+          const float* q = recv + (sl * srows + lr) * EP_LD + i;
+          s += q[0];
+          if (sw) su += q[per * EP_LD];
+        }
+      }
+      v[u] = sw ? swiglu_clamped(s, su, p.clamp) : s;
+    }
+#pragma unroll
+    for (int u = 0; u < B; ++u) {
+      if (!ok[u]) continue;
+      switch (p.epi) {
+        case EPI_BF16:
+          reinterpret_cast<__nv_bfloat16*>(p.out)[o[u]] = __float2bfloat16_rn(v[u]);
+          break;
+        case EPI_F16:
+        case EPI_SWIGLU_F16:
+          reinterpret_cast<__half*>(p.out)[o[u]] = bf16_as_f16(v[u]);
+          break;
+        case EPI_RESID_BF16:
+          reinterpret_cast<__nv_bfloat16*>(p.out)[o[u]] = __float2bfloat16_rn(r[u] + v[u]);
+          break;
+        default:
+          reinterpret_cast<float*>(p.out)[o[u]] = v[u];
+          break;
+      }
+    }
+  }
 }
 
 // E8M0 byte -> 2^(e-127) for e in 1..254 by placing the byte in the f32 exponent field
@@ -584,44 +659,55 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    // K-split tiles: the peers must have finished reading this CTA's previous partial
-    if (clustered && tiles_done > 0 &&
-        !pipe_wait<true>(red_done, (tiles_done - 1) & 1, p.status, abort))
-      return;
-    const int m0 = 16 * mt + g;
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      if (NT == 1 || t < ntl) {
-        const int col = t * 8 + 2 * c;
-        ep_mine[m0 * L::EP_LD + col] = acc[t][0];
-        ep_mine[m0 * L::EP_LD + col + 1] = acc[t][1];
-        ep_mine[(m0 + 8) * L::EP_LD + col] = acc[t][2];
-        ep_mine[(m0 + 8) * L::EP_LD + col + 1] = acc[t][3];
-      }
-    }
-    if (*abort) return;
-    if (KS > 1) {  // the K shares' tiles, added in a fixed order
-      consumer_bar<NTHR>();
-      const int cols = ntl * 8;
-      for (int idx = tid; idx < TILE_M * cols; idx += NTHR) {
-        const int m = idx / cols, col = idx - m * cols;
-        float v = ep[m * L::EP_LD + col];
-#pragma unroll
-        for (int k = 1; k < KS; ++k) v += ep[k * TILE_M * L::EP_LD + m * L::EP_LD + col];
-        ep[m * L::EP_LD + col] = v;
-      }
-    }
     if (clustered) {
-      fence_acq_rel_cluster();
+      write_partial<NT, L::EP_LD>(acc, ep_mine, mt, g, c, ntl);
+      if (*abort) return;
+      if (KS > 1) {
+        consumer_bar<NTHR>();
+        sum_kshares<KS, L::EP_LD, NTHR>(ep, ntl, tid);
+      }
+      fence_proxy_async_shared();  // the partial is read by bulk copies next
       consumer_bar<NTHR>();
-      if (tid < p.ksplit) mbar_arrive_remote(mapa_shared(smem_u32(red_full), tid));  // one lane per rank
-      if (!pipe_wait<true>(red_full, tiles_done & 1, p.status, abort)) return;
-      epilogue_cluster<L::EP_LD, NTHR>(p, it, ep, tid, rank, p.ksplit, red_done);
+      float* recv = ep + KS * L::EP_TILE;
+      if (tid == 0) {
+        // every owner must have emptied its receive tile of the previous K-split tile
+        if (tiles_done > 0 && !pipe_wait<true>(red_done, (tiles_done - 1) & 1, p.status, abort))
+          return;
+        push_slices<L::EP_LD>(p, ep, recv, red_full, rank, it.n);
+      }
+      if (!pipe_wait(red_full, tiles_done & 1, p.status, abort)) return;
+      owner_epilogue<L::EP_LD, NTHR>(p, it, recv, tid, rank);
+      if (tid == 0) bulk_wait_read();  // this CTA's pushes have read its partial tile
+      consumer_bar<NTHR>();
+      if (tid < p.ksplit) mbar_arrive_remote(mapa_shared(smem_u32(red_done), tid));  // tile free
     } else {
+      const int m0 = 16 * mt + g;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        if (NT == 1 || t < ntl) {
+          const int col = t * 8 + 2 * c;
+          ep_mine[m0 * L::EP_LD + col] = acc[t][0];
+          ep_mine[m0 * L::EP_LD + col + 1] = acc[t][1];
+          ep_mine[(m0 + 8) * L::EP_LD + col] = acc[t][2];
+          ep_mine[(m0 + 8) * L::EP_LD + col + 1] = acc[t][3];
+        }
+      }
+      if (*abort) return;
+      if (KS > 1) {  // the K shares' tiles, added in a fixed order
+        consumer_bar<NTHR>();
+        const int cols = ntl * 8;
+        for (int idx = tid; idx < TILE_M * cols; idx += NTHR) {
+          const int m = idx / cols, col = idx - m * cols;
+          float v = ep[m * L::EP_LD + col];
+#pragma unroll
+          for (int k = 1; k < KS; ++k) v += ep[k * TILE_M * L::EP_LD + m * L::EP_LD + col];
+          ep[m * L::EP_LD + col] = v;
+        }
+      }
       consumer_bar<NTHR>();
       epilogue_local<L::EP_LD, NTHR>(p, it, ep, tid);
+      consumer_bar<NTHR>();  // the tile is written out before the next partial overwrites it
     }
-    consumer_bar<NTHR>();  // the tile is written out before the next partial overwrites it
     ++tiles_done;
   }
   // no peer may still be reading this CTA's shared memory when it exits
@@ -648,7 +734,7 @@ __global__ void __launch_bounds__(gemm_threads(KS), FMT == 4 ? 3 : 2)
       mbar_init(&full[s], 1 + 32);  // expect_tx arrival + one cp.async arrival per lane
       mbar_init(&empty[s], CONSUMER_WARPS);
     }
-    mbar_init(red_full, clustered ? p.ksplit : 1);
+    mbar_init(red_full, 1);  // the owner's expect_tx arrival; the peers' slices complete_tx
     mbar_init(red_done, clustered ? p.ksplit : 1);
     fence_mbar_init();
     *abort = 0;

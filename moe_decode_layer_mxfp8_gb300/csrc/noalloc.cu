@@ -94,17 +94,14 @@ extern "C" int mono_attention_noalloc(const mono_layer_spec* s, const void* q, v
   int rc = scratch_for_current_device(&base, &sms);
   if (rc != MONO_OK) return rc;
 
-  // Same split choice as a layer step, reduced if the partials would not fit; a problem
-  // that does not fit even at the fewest splits the window allows is refused.
+  // Same split choice as a layer step (one split per 128 window keys); a problem whose
+  // partials do not fit the scratch array is refused.
   const int width = std::max(s->causal ? s->window : s->swa_width, s->window);
-  const int min_splits = (width + 127) / 128;
-  const int want = (2 * sms + rows * G - 1) / (rows * G);
-  int splits = std::max(min_splits, std::min(8, want));
+  const int splits = (width + 127) / 128;
   auto part_bytes = [&](int S) {
-    return (size_t)rows * s->n_q_heads * S * (s->head_dim + 2) * sizeof(float);
+    return (size_t)rows * s->n_q_heads * S * (s->head_dim + ATTN_PART_HEAD) * sizeof(float);
   };
   const size_t cap = MONO_NOALLOC_SCRATCH_BYTES - kPartOff;
-  while (splits > min_splits && part_bytes(splits) > cap) --splits;
   if (splits > 1 && part_bytes(splits) > cap) return MONO_ERR_TOO_MANY_ROWS;
 
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
