@@ -5,40 +5,46 @@ namespace mono {
 
 namespace {
 
-// Ring depth and K-shares per variant: dense matrices (few CTAs per SM) give each stage to
-// two warps per M-tile; the routed experts fill the SMs with CTAs instead.
-template <int FMT, int NT>
+// Ring depth per variant.  Dense matrices (few CTAs per SM) give each stage to two warps
+// per M-tile; the routed experts fill the SMs with CTAs instead, except in small steps,
+// whose few expert items also split K across a cluster.
+template <int FMT, int NT, int KS>
 struct Var;
-template <> struct Var<8, 1> { static constexpr int NSTAGE = 6, KS = 2; };
-template <> struct Var<8, 2> { static constexpr int NSTAGE = 6, KS = 2; };
-template <> struct Var<8, 4> { static constexpr int NSTAGE = 4, KS = 2; };
-template <> struct Var<8, 6> { static constexpr int NSTAGE = 3, KS = 2; };
-template <> struct Var<4, 1> { static constexpr int NSTAGE = 4, KS = 1; };
+template <> struct Var<8, 1, 2> { static constexpr int NSTAGE = 6; };
+template <> struct Var<8, 2, 2> { static constexpr int NSTAGE = 6; };
+template <> struct Var<8, 4, 2> { static constexpr int NSTAGE = 4; };
+template <> struct Var<8, 6, 2> { static constexpr int NSTAGE = 3; };
+template <> struct Var<4, 1, 1> { static constexpr int NSTAGE = 4; };
+template <> struct Var<4, 1, 2> { static constexpr int NSTAGE = 4; };
 
-template <int FMT, int NT>
+template <int FMT, int NT, int KS>
 constexpr int smem_of() {
-  return GemmLayout<FMT, NT, Var<FMT, NT>::NSTAGE, Var<FMT, NT>::KS>::BYTES;
+  return GemmLayout<FMT, NT, Var<FMT, NT, KS>::NSTAGE, KS>::BYTES;
 }
 
-template <int FMT, int NT>
-void* kernel_of() {
-  return reinterpret_cast<void*>(&mx_gemm_kernel<FMT, NT, Var<FMT, NT>::NSTAGE, Var<FMT, NT>::KS>);
+template <int FMT, int NT, int KS>
+void* kernel_of(int* smem, int* threads) {
+  *smem = smem_of<FMT, NT, KS>();
+  *threads = gemm_threads(KS);
+  return reinterpret_cast<void*>(&mx_gemm_kernel<FMT, NT, Var<FMT, NT, KS>::NSTAGE, KS>);
 }
+
+int ks_of(GemmVariant v) { return v.ks ? v.ks : (v.fmt == 8 ? 2 : 1); }
 
 void* variant_kernel(GemmVariant v, int* smem, int* threads) {
-  if (v.fmt == 8) {
+  const int ks = ks_of(v);
+  if (v.fmt == 8 && ks == 2) {
     switch (v.nt) {
-      case 1: *smem = smem_of<8, 1>(); *threads = gemm_threads(Var<8, 1>::KS); return kernel_of<8, 1>();
-      case 2: *smem = smem_of<8, 2>(); *threads = gemm_threads(Var<8, 2>::KS); return kernel_of<8, 2>();
-      case 4: *smem = smem_of<8, 4>(); *threads = gemm_threads(Var<8, 4>::KS); return kernel_of<8, 4>();
-      case 6: *smem = smem_of<8, 6>(); *threads = gemm_threads(Var<8, 6>::KS); return kernel_of<8, 6>();
+      case 1: return kernel_of<8, 1, 2>(smem, threads);
+      case 2: return kernel_of<8, 2, 2>(smem, threads);
+      case 4: return kernel_of<8, 4, 2>(smem, threads);
+      case 6: return kernel_of<8, 6, 2>(smem, threads);
       default: return nullptr;
     }
   }
   if (v.fmt == 4 && v.nt == 1) {
-    *smem = smem_of<4, 1>();
-    *threads = gemm_threads(Var<4, 1>::KS);
-    return kernel_of<4, 1>();
+    if (ks == 1) return kernel_of<4, 1, 1>(smem, threads);
+    if (ks == 2) return kernel_of<4, 1, 2>(smem, threads);
   }
   return nullptr;
 }
@@ -106,11 +112,10 @@ int gemm_max_clusters(GemmVariant v, int cluster) {
   return n;
 }
 
-template <int FMT, int NT>
+template <int FMT, int NT, int KS>
 cudaError_t launch_variant(const cudaLaunchConfig_t& cfg, const CUtensorMap& map,
                            const GemmParams& p) {
-  return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<FMT, NT, Var<FMT, NT>::NSTAGE, Var<FMT, NT>::KS>,
-                            map, p);
+  return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<FMT, NT, Var<FMT, NT, KS>::NSTAGE, KS>, map, p);
 }
 
 cudaError_t launch_gemm(const Launch& L, GemmVariant v, const CUtensorMap& map,
@@ -121,13 +126,13 @@ cudaError_t launch_gemm(const Launch& L, GemmVariant v, const CUtensorMap& map,
   const cudaLaunchConfig_t cfg = config(L, grid, t, smem, cluster, attr);
   if (v.fmt == 8) {
     switch (v.nt) {
-      case 1: return launch_variant<8, 1>(cfg, map, p);
-      case 2: return launch_variant<8, 2>(cfg, map, p);
-      case 4: return launch_variant<8, 4>(cfg, map, p);
-      default: return launch_variant<8, 6>(cfg, map, p);
+      case 1: return launch_variant<8, 1, 2>(cfg, map, p);
+      case 2: return launch_variant<8, 2, 2>(cfg, map, p);
+      case 4: return launch_variant<8, 4, 2>(cfg, map, p);
+      default: return launch_variant<8, 6, 2>(cfg, map, p);
     }
   }
-  return launch_variant<4, 1>(cfg, map, p);
+  return ks_of(v) == 2 ? launch_variant<4, 1, 2>(cfg, map, p) : launch_variant<4, 1, 1>(cfg, map, p);
 }
 
 }  // namespace mono

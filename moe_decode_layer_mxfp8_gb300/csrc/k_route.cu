@@ -3,9 +3,10 @@
 //
 // router_kernel: z[r, e] = u[r] . W_r[e] in f32, split over K: CTA (4 experts, 1024-wide K
 // slice) holds its experts' weight slices in registers (fetched before waiting on the
-// previous kernel), reads the slice of every row of u and writes one partial per (slice,
-// row, expert).  Rows go two at a time: two independent FMA chains per lane, then one
-// transposing butterfly that leaves each half-warp with one row's sum.
+// previous kernel), stages the slice of every row of u in shared memory and writes one
+// partial per (slice, row, expert).  Rows go eight at a time: eight independent FMA chains
+// per lane, then one transposing butterfly that leaves each of eight lanes with one row's
+// sum.
 //
 // topk_kernel sums the partials in slice order (a fixed order, so results replay
 // bit-exactly) into shared memory, picks the top-k per row (a warp per row: the largest key
@@ -24,7 +25,9 @@ constexpr int RT_THREADS = RT_EXPERTS * 32;
 constexpr int RT_J = ROUTER_KSLICE / 128;  // float4 weight chunks per lane
 constexpr int MAX_ROWS = 48, MAX_K = 8;
 
-__global__ void __launch_bounds__(RT_THREADS, 8) router_kernel(RouterArgs a) {
+__global__ void __launch_bounds__(RT_THREADS) router_kernel(RouterArgs a) {
+  extern __shared__ __align__(16) uint8_t rt_smem[];
+  __half* us = reinterpret_cast<__half*>(rt_smem);  // [rows][ROUTER_KSLICE]
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int k0 = blockIdx.y * ROUTER_KSLICE;
@@ -38,44 +41,57 @@ __global__ void __launch_bounds__(RT_THREADS, 8) router_kernel(RouterArgs a) {
                 ? *reinterpret_cast<const float4*>(a.wr + (size_t)e * a.H + k0 + 128 * j + 4 * lane)
                 : make_float4(0.f, 0.f, 0.f, 0.f);
   pdl_wait();
+  const int chunks = klen / 8;  // 16-byte chunks per row
+  for (int idx = tid; idx < a.rows * chunks; idx += RT_THREADS) {
+    const int r = idx / chunks, c = idx - r * chunks;
+    cp_async16(us + r * ROUTER_KSLICE + c * 8, a.u + (size_t)r * a.H + k0 + c * 8, 16);
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
   if (e >= a.E) return;
-  // u is read straight from L2 through L1 (the CTA's four warps read the same values), so
-  // the kernel needs no shared memory and, at 64 registers or fewer, fits beside the shared
-  // expert's GEMM CTAs.  Lane l ends a pair of rows with the sum of row bit4(l).
-  for (int r0 = 0; r0 < a.rows; r0 += 2) {
-    uint2 uv[2][RT_J];
+  // lane l ends a group of eight rows with the sum of row 4 bit4(l) + 2 bit3(l) + bit2(l)
+  const int my_row = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+  for (int r0 = 0; r0 < a.rows; r0 += 8) {
+    float acc[8];
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-      for (int j = 0; j < RT_J; ++j)
-        uv[i][j] = r0 + i < a.rows && 128 * j < klen
-                       ? __ldg(reinterpret_cast<const uint2*>(a.u + (size_t)(r0 + i) * a.H + k0 +
-                                                              128 * j + 4 * lane))
-                       : make_uint2(0u, 0u);
-    float acc[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 8; ++i) {
       acc[i] = 0.0f;
+      if (r0 + i < a.rows) {
+        const __half* ur = us + (r0 + i) * ROUTER_KSLICE + 4 * lane;
 #pragma unroll
-      for (int j = 0; j < RT_J; ++j) {
-        const float2 u0 = __half22float2(*reinterpret_cast<const __half2*>(&uv[i][j].x));
-        const float2 u1 = __half22float2(*reinterpret_cast<const __half2*>(&uv[i][j].y));
-        acc[i] = fmaf(u0.x, wv[j].x, acc[i]);
-        acc[i] = fmaf(u0.y, wv[j].y, acc[i]);
-        acc[i] = fmaf(u1.x, wv[j].z, acc[i]);
-        acc[i] = fmaf(u1.y, wv[j].w, acc[i]);
+        for (int j = 0; j < RT_J; ++j) {
+          if (128 * j < klen) {
+            const uint2 uv = lds64(ur + 128 * j);
+            const float2 u0 = __half22float2(*reinterpret_cast<const __half2*>(&uv.x));
+            const float2 u1 = __half22float2(*reinterpret_cast<const __half2*>(&uv.y));
+            acc[i] = fmaf(u0.x, wv[j].x, acc[i]);
+            acc[i] = fmaf(u0.y, wv[j].y, acc[i]);
+            acc[i] = fmaf(u1.x, wv[j].z, acc[i]);
+            acc[i] = fmaf(u1.y, wv[j].w, acc[i]);
+          }
+        }
       }
     }
-    // transposing butterfly: 2 values over 32 lanes -> 1 row sum per lane (5 shuffles)
-    const bool b4 = lane & 16;
-    float v = (b4 ? acc[1] : acc[0]) + __shfl_xor_sync(0xffffffffu, b4 ? acc[0] : acc[1], 16);
-    v += __shfl_xor_sync(0xffffffffu, v, 8);
-    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    // transposing butterfly: 8 values over 32 lanes -> 1 row sum per lane (9 shuffles)
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float s4[4], s3[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float send = b4 ? acc[i] : acc[i + 4];
+      const float keep = b4 ? acc[i + 4] : acc[i];
+      s4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float send = b3 ? s4[i] : s4[i + 2];
+      const float keep = b3 ? s4[i + 2] : s4[i];
+      s3[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    float v = (b2 ? s3[1] : s3[0]) + __shfl_xor_sync(0xffffffffu, b2 ? s3[0] : s3[1], 4);
     v += __shfl_xor_sync(0xffffffffu, v, 2);
     v += __shfl_xor_sync(0xffffffffu, v, 1);
-    const int my_row = r0 + (b4 ? 1 : 0);
-    if ((lane & 15) == 0 && my_row < a.rows)
-      a.partial[((size_t)blockIdx.y * a.rows + my_row) * a.E + e] = v;
+    if ((lane & 3) == 0 && r0 + my_row < a.rows)
+      a.partial[((size_t)blockIdx.y * a.rows + r0 + my_row) * a.E + e] = v;
   }
 }
 
@@ -221,19 +237,23 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
 
 }  // namespace
 
+int router_smem_bytes(int rows) { return rows * ROUTER_KSLICE * 2; }
 // The logits of the step in shared memory, [rows][E].
 int topk_smem_bytes() { return MAX_ROWS * MAX_EXPERTS * 4; }
 
-// The limit is a property of the kernel, shared by every layer handle of the process: set it
-// for the largest step any handle accepts.
+// The limits are properties of the kernels, shared by every layer handle of the process: set
+// them for the largest step any handle accepts.
 cudaError_t router_prepare() {
+  cudaError_t e = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       router_smem_bytes(MAX_ROWS));
+  if (e != cudaSuccess) return e;
   return cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               topk_smem_bytes());
 }
 
 cudaError_t launch_router(const Launch& L, const RouterArgs& a) {
   const dim3 grid((a.E + RT_EXPERTS - 1) / RT_EXPERTS, (a.H + ROUTER_KSLICE - 1) / ROUTER_KSLICE);
-  return launch_ex(L, grid, dim3(RT_THREADS), 0, router_kernel, a);
+  return launch_ex(L, grid, dim3(RT_THREADS), router_smem_bytes(a.rows), router_kernel, a);
 }
 
 cudaError_t launch_topk(const Launch& L, const TopkArgs& a) {

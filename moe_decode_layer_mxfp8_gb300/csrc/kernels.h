@@ -123,6 +123,7 @@ cudaError_t launch_final(const Launch&, const FinalArgs&);
 // MX GEMM variants: fmt 8 (MXFP8) with nt in {1, 2, 4, 6}; fmt 4 (MXFP4) with nt 1.
 struct GemmVariant {
   int fmt, nt;
+  int ks = 0;  // K-share warps per M-tile; 0: the format's default (dense 2, experts 1)
 };
 int gemm_smem_bytes(GemmVariant v);
 cudaError_t gemm_prepare(GemmVariant v);  // raises the dynamic shared-memory limit

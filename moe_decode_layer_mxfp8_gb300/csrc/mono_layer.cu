@@ -60,7 +60,8 @@ struct mono_layer {
   DensePlan dense[D_COUNT];
   CUtensorMap map_ex_gu, map_ex_d;
   int ctas_gemm8[7] = {};  // by nt
-  int ctas_gemm4 = 0;
+  int ex_ctas = 0;      // persistent CTAs of the expert GEMM (large steps)
+  int ex_clusters = 0;  // clusters of EXPERT_CLUSTER CTAs of the K-splitting expert GEMM
   int attn_min_splits = 1;
   cudaEvent_t prof[kLaunchesPerStep + 1] = {};
   bool profiling = false;
@@ -278,8 +279,13 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
       if (d.max_clusters[nt] < 1) rc = MONO_ERR_CUDA;
     }
   }
-  if (gemm_prepare({4, 1}) != cudaSuccess) rc = MONO_ERR_CUDA;
-  h->ctas_gemm4 = std::max(1, gemm_ctas_per_sm({4, 1}));
+  if (gemm_prepare({4, 1, 1}) != cudaSuccess || gemm_prepare({4, 1, 2}) != cudaSuccess)
+    rc = MONO_ERR_CUDA;
+  h->ex_ctas = h->num_sms * std::max(1, gemm_ctas_per_sm({4, 1, 1}));
+  // a margin of clusters below the empty-GPU maximum, so that every cluster is resident at
+  // once even while the previous kernels' last CTAs drain (items are assigned statically)
+  h->ex_clusters = gemm_max_clusters({4, 1, 2}, EXPERT_CLUSTER) * 7 / 8;
+  if (h->ex_clusters < 1) rc = MONO_ERR_CUDA;
   if (attention_prepare(s.head_dim) != cudaSuccess) rc = MONO_ERR_CUDA;
   if (router_prepare() != cudaSuccess) rc = MONO_ERR_CUDA;
   if (!rc && (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
@@ -429,7 +435,9 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     p.act_ld = act_ld;
     p.act_rowmap = rowmap;
     p.n_tiles = n_tiles;
-    p.ksplit = 1;
+    // small steps: clusters that split the K of each item when the items are few
+    const bool small = R * K <= EXPERT_SMALL_SLOTS;
+    p.ksplit = small ? EXPERT_CLUSTER : 1;
     p.n_slots = R * K;
     p.route = h->route;
     p.epi = epi;
@@ -437,7 +445,9 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     p.out_ld = out_ld;
     p.clamp = s.swiglu_clamp;
     p.status = h->status;
-    return launch_gemm(L, {4, 1}, map, p, h->num_sms * h->ctas_gemm4, 1);
+    if (small)
+      return launch_gemm(L, {4, 1, 2}, map, p, h->ex_clusters * EXPERT_CLUSTER, EXPERT_CLUSTER);
+    return launch_gemm(L, {4, 1, 1}, map, p, h->ex_ctas, 1);
   };
 
   // ---------------------------------------------------------------- K1: attention front

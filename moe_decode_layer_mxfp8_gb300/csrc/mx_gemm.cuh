@@ -40,6 +40,8 @@ constexpr int W_STAGE_BYTES = TILE_M * BOX_BYTES;
 // M-tile each take 1/KS of every stage's K blocks), plus the producer warp.
 __host__ __device__ constexpr int gemm_threads(int ks) { return (4 * ks + 1) * 32; }
 constexpr int MAX_CLUSTER = 8;
+constexpr int EXPERT_CLUSTER = 4;       // CTAs per cluster of the K-splitting expert GEMM
+constexpr int EXPERT_SMALL_SLOTS = 24;  // routed (row, slot) pairs of a step that uses it
 
 // Routing metadata written by the top-k kernel and read by the expert GEMMs.
 struct RouteInfo {
@@ -112,9 +114,9 @@ struct GemmLayout {
   static constexpr int ACT_OFF = NSTAGE * W_STAGE_BYTES;
   static constexpr int SC_OFF = ACT_OFF + NSTAGE * ACT_BYTES;
   static constexpr int EP_OFF = align_up(SC_OFF + NSTAGE * SC_BYTES, 16);
-  // one partial tile per K share, then (dense matrices) the K-split receive tile
+  // one partial tile per K share, then the K-split receive tile
   static constexpr int EP_TILE = TILE_M * EP_LD;  // floats
-  static constexpr int EP_BYTES = (KS + (EXPERT ? 0 : 1)) * EP_TILE * 4;
+  static constexpr int EP_BYTES = (KS + 1) * EP_TILE * 4;
   static constexpr int ROUTE_OFF = align_up(EP_OFF + EP_BYTES, 16);
   static constexpr int ROUTE_BYTES = EXPERT ? (int)sizeof(RouteSmem) : 0;
   static constexpr int BAR_OFF = align_up(ROUTE_OFF + ROUTE_BYTES, 16);
@@ -134,11 +136,31 @@ struct Item {
   int col0;            // first output column
 };
 
+// Work items of a launch: with ks > 1 every (tile or expert item) is split over the ks CTAs
+// of a cluster along K, virtual item q = item * ks + split.
+__device__ __forceinline__ int expert_items(const GemmParams& p, const RouteSmem* rs) {
+  return rs->rg_prefix[rs->n_hit] * p.n_tiles;
+}
+// Routed experts split K across the cluster only when there are too few items to fill the
+// grid's clusters twice (one-token and draft steps); dense matrices always do.
+__device__ __forceinline__ int split_of(const GemmParams& p, const RouteSmem* rs) {
+  if (p.ksplit <= 1) return 1;
+  if (!rs) return p.ksplit;
+  return expert_items(p, rs) <= 2 * (int)(gridDim.x / p.ksplit) ? p.ksplit : 1;
+}
+
 template <int FMT>
 __device__ __forceinline__ void decode_item(const GemmParams& p, const RouteSmem* rs, int q,
-                                            Item& it) {
+                                            int ks, Item& it) {
   constexpr int KC = FmtTraits<FMT>::KC;
   int base = 0;
+  it.split = q % ks;
+  q /= ks;
+  const int nck_all = (p.K + KC - 1) / KC;
+  const int cps = (nck_all + ks - 1) / ks;
+  const int c0 = it.split * cps;
+  it.nck = max(0, min(cps, nck_all - c0));
+  it.k0 = c0 * KC;
   if (rs) {
     int lo = 0, hi = rs->n_hit - 1;
     while (lo < hi) {
@@ -150,20 +172,11 @@ __device__ __forceinline__ void decode_item(const GemmParams& p, const RouteSmem
     const int local = q - rs->rg_prefix[d] * p.n_tiles;
     it.tile = local / rgc;
     const int rg = local - it.tile * rgc;
-    it.split = 0;
     base = rs->hit_e[d] * p.rows_per_mat;
     it.n = min(EXPERT_ROWS, rs->hit_cnt[d] - rg * EXPERT_ROWS);
     it.row0 = rs->hit_off[d] + rg * EXPERT_ROWS;
-    it.k0 = 0;
-    it.nck = (p.K + KC - 1) / KC;
   } else {
-    it.tile = q / p.ksplit;
-    it.split = q - it.tile * p.ksplit;
-    const int nck_all = (p.K + KC - 1) / KC;
-    const int cps = (nck_all + p.ksplit - 1) / p.ksplit;
-    const int c0 = it.split * cps;
-    it.nck = max(0, min(cps, nck_all - c0));
-    it.k0 = c0 * KC;
+    it.tile = q;
     it.n = p.dense_rows;
     it.row0 = 0;
   }
@@ -190,8 +203,8 @@ __device__ __forceinline__ void decode_item(const GemmParams& p, const RouteSmem
   }
 }
 
-__device__ __forceinline__ int total_items(const GemmParams& p, const RouteSmem* rs) {
-  return rs ? rs->rg_prefix[rs->n_hit] * p.n_tiles : p.n_tiles * p.ksplit;
+__device__ __forceinline__ int total_items(const GemmParams& p, const RouteSmem* rs, int ks) {
+  return (rs ? expert_items(p, rs) : p.n_tiles) * ks;
 }
 
 template <int NTHR>
@@ -295,9 +308,10 @@ template <int FMT, int NT, int NSTAGE, int KS>
 __device__ int prefetch_weights(const GemmParams& p, const CUtensorMap* map, uint8_t* smem,
                                 uint64_t* full) {
   const int lane = threadIdx.x & 31;
-  if (p.route || (int)blockIdx.x >= total_items(p, nullptr)) return 0;
+  const int ks = split_of(p, nullptr);
+  if (p.route || (int)blockIdx.x >= total_items(p, nullptr, ks)) return 0;
   Item it;
-  decode_item<FMT>(p, nullptr, blockIdx.x, it);
+  decode_item<FMT>(p, nullptr, blockIdx.x, ks, it);
   const int pre = min(NSTAGE, it.nck);
   for (int c = 0; c < pre; ++c) issue_weights<FMT, NT, NSTAGE, KS>(p, map, smem, full, it, c, c, lane);
   return pre;
@@ -308,11 +322,12 @@ __device__ void gemm_producer(const GemmParams& p, const RouteSmem* rs, const CU
                               uint8_t* smem, uint64_t* full, uint64_t* empty,
                               volatile int* abort, int pre) {
   const int lane = threadIdx.x & 31;
-  const int n_items = total_items(p, rs);
+  const int ks = split_of(p, rs);
+  const int n_items = total_items(p, rs, ks);
   int iter = 0;
   for (int q = blockIdx.x; q < n_items; q += gridDim.x) {
     Item it;
-    decode_item<FMT>(p, rs, q, it);
+    decode_item<FMT>(p, rs, q, ks, it);
     for (int c = 0; c < it.nck; ++c, ++iter) {
       const int s = iter % NSTAGE;
       const uint32_t ph = (iter / NSTAGE) & 1;
@@ -545,13 +560,14 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
 #pragma unroll
   for (int j = 0; j < (FMT == 4 ? HB : 2 * HB); ++j)
     offs[j] = (((FMT == 4 ? kh * HB : 2 * kh * HB) + j) ^ g) * 16 + c * 4;
-  const int n_items = total_items(p, rs);
-  const bool clustered = rs == nullptr && p.ksplit > 1;
+  const int ks = split_of(p, rs);
+  const int n_items = total_items(p, rs, ks);
+  const bool clustered = ks > 1;
   const uint32_t rank = clustered ? cluster_ctarank() : 0u;
   int iter = 0, tiles_done = 0;
   for (int q = blockIdx.x; q < n_items; q += gridDim.x) {
     Item it;
-    decode_item<FMT>(p, rs, q, it);
+    decode_item<FMT>(p, rs, q, ks, it);
     const int ntl = (it.n + 7) >> 3;
     float acc[NT][4];
 #pragma unroll
@@ -728,7 +744,7 @@ __global__ void __launch_bounds__(gemm_threads(KS), FMT == 4 ? 3 : 2)
   uint64_t* red_done = red_full + 1;
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::MISC_OFF);
   const int warp = threadIdx.x >> 5;
-  const bool clustered = p.route == nullptr && p.ksplit > 1;
+  const bool clustered = p.ksplit > 1;  // a cluster launch (routed experts may still not split)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&full[s], 1 + 32);  // expect_tx arrival + one cp.async arrival per lane
