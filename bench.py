@@ -370,6 +370,43 @@ def _workload_desc(name, spec, rows):
             f"(moe {spec['moe_inter']}, shared {spec['shared_inter']})")
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the dominant
+# kernel, from the ncu capture summarised in profiles/expert_gate_up_full_r48.md, keyed by
+# the md5 of the GEMM sources it was taken on: reported only while those are unchanged.
+NCU_TRAFFIC = {
+    ("full_r48", "expert_gate_up"): (499_417_088, "35ab6c4540fb050b076769dea45c17b0"
+                                                  "d8cc55517e409104957990358e50ec40"
+                                                  "0d5ea4d34680824b9da5edc280a0c7a8"),
+}
+
+
+def _gemm_source_hash():
+    import hashlib
+    d = os.path.join(os.path.dirname(os.path.abspath(__file__)), "moe_decode_layer_mxfp8_gb300", "csrc")
+    return "".join(hashlib.md5(open(os.path.join(d, f), "rb").read()).hexdigest()
+                   for f in ("mx_gemm.cuh", "k_gemm.cu", "common.cuh"))
+
+
+def run_eager(name, n):
+    """N eager layer steps (launch order: per step 15 launches, see mono_layer_launch_name)."""
+    from moe_decode_layer_mxfp8_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    spec, step, layers = _layer_copies(name, 1, dev)
+    out = torch.empty_like(step["x"])
+    stream = torch.cuda.Stream(dev)
+    lay = layers[0][0]
+    with torch.cuda.stream(stream):
+        for _ in range(n):
+            lay.step(step["x"], out, step["positions"], step["row_req"], step["block_table"],
+                     step["kv_cache"], stream=stream)
+    torch.cuda.synchronize(dev)
+    if lay.status() != 0:
+        raise SystemExit(f"layer status {lay.status()}")
+    print(json.dumps({"eager_steps": n, "workload": name, "rows": step["rows"]}))
+
+
 # ------------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -380,8 +417,14 @@ def main():
     ap.add_argument("--no-sweep", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--workload", default=HEADLINE, choices=["full_r48", "full_r1", "draft_r6"])
+    ap.add_argument("--eager", type=int, default=0, metavar="N",
+                    help="only run N eager steps of the workload (one layer copy) and exit: the "
+                         "command the ncu captures under profiles/ run")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.eager:
+        run_eager(args.workload, args.eager)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -452,6 +495,10 @@ def main():
         roof = dict(kernel=top, bound="hbm", achieved=round(ach, 1), peak=peak,
                     peak_kind=peak_kind, unit="GB/s", frac=round(ach / peak, 4),
                     traffic=None, bytes_per_launch=int(alg), us_per_launch=round(prof[top], 2))
+        t = NCU_TRAFFIC.get((args.workload, top))
+        if t is not None and t[1] == _gemm_source_hash():
+            roof["traffic"] = t[0]
+            roof["traffic_source"] = "profiles/expert_gate_up_full_r48.md (ncu, one launch)"
     total_prof = sum(prof.values())
     gbs = res["bytes"] / res["us"] / 1e3
     line = dict(
