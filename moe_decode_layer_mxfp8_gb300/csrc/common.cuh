@@ -117,6 +117,20 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
 __device__ __forceinline__ void st_dsmem_f32(uint32_t cluster_addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
 }
+// Raises an mbarrier's expected transaction count without arriving.
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// Bulk copy global -> this CTA's shared memory, completing `bytes` on its mbarrier.
+// Addresses and size multiples of 16.
+__device__ __forceinline__ void bulk_load_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
 // Bulk copy from this CTA's shared memory to (possibly) another CTA's of the cluster,
 // completing `bytes` on the destination's mbarrier.  Addresses and size multiples of 16.
 __device__ __forceinline__ void bulk_copy_s2s(uint32_t dst_cluster, const void* src,

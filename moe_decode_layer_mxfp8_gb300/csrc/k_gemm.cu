@@ -14,7 +14,7 @@ template <> struct Var<8, 1, 2> { static constexpr int NSTAGE = 6; };
 template <> struct Var<8, 2, 2> { static constexpr int NSTAGE = 6; };
 template <> struct Var<8, 4, 2> { static constexpr int NSTAGE = 4; };
 template <> struct Var<8, 6, 2> { static constexpr int NSTAGE = 3; };
-template <> struct Var<4, 1, 1> { static constexpr int NSTAGE = 4; };
+template <> struct Var<4, 1, 1> { static constexpr int NSTAGE = 3; };  // 4 CTAs per SM
 template <> struct Var<4, 1, 2> { static constexpr int NSTAGE = 4; };
 
 template <int FMT, int NT, int KS>

@@ -290,16 +290,30 @@ __device__ __forceinline__ void issue_acts(const GemmParams& p, const RouteSmem*
   const int k0 = it.k0 + c * KC;
   const int vbytes = min(KC, p.K - k0) * 2;
   uint8_t* ast = smem + L::ACT_OFF + s * L::ACT_BYTES;
-  for (int idx = lane; idx < it.n * CPR; idx += 32) {
-    const int i = idx / CPR, ch = idx - i * CPR;
-    int arow = i;
-    if (rs) arow = p.act_rowmap ? rs->rowmap[it.row0 + i] : it.row0 + i;
-    const bool ok = ch * 16 < vbytes;
-    const __half* src = p.act + (long long)arow * p.act_ld + k0 + ch * 8;
-    cp_async16(ast + i * ASTR + ch * 16, ok ? (const void*)src : (const void*)p.act,
-               ok ? 16u : 0u);
+  if (FMT == 4 && vbytes == KC * 2) {
+    // expert rows (<= 8 of 512 bytes): one bulk copy per row, counted on the stage's barrier
+    // before any lane's arrival below can complete the phase.  (The dense matrices' up to 48
+    // rows of 256 bytes stream faster as 16-byte copies spread over the lanes.)
+    if (lane == 0) mbar_expect_tx(&full[s], (uint32_t)(it.n * vbytes));
+    __syncwarp();
+    for (int i = lane; i < it.n; i += 32) {
+      int arow = i;
+      if (rs) arow = p.act_rowmap ? rs->rowmap[it.row0 + i] : it.row0 + i;
+      bulk_load_g2s(ast + i * ASTR, p.act + (long long)arow * p.act_ld + k0, (uint32_t)vbytes,
+                    &full[s]);
+    }
+  } else {  // 16-byte copies, zero-filled past the end of K
+    for (int idx = lane; idx < it.n * CPR; idx += 32) {
+      const int i = idx / CPR, ch = idx - i * CPR;
+      int arow = i;
+      if (rs) arow = p.act_rowmap ? rs->rowmap[it.row0 + i] : it.row0 + i;
+      const bool ok = ch * 16 < vbytes;
+      const __half* src = p.act + (long long)arow * p.act_ld + k0 + ch * 8;
+      cp_async16(ast + i * ASTR + ch * 16, ok ? (const void*)src : (const void*)p.act,
+                 ok ? 16u : 0u);
+    }
   }
-  cp_async_arrive_noinc(&full[s]);
+  cp_async_arrive_noinc(&full[s]);  // after this lane's scale copies (and any above) land
 }
 
 // The first item's first stages whose weights are issued before griddepcontrol.wait (dense
@@ -731,7 +745,7 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
 }
 
 template <int FMT, int NT, int NSTAGE, int KS>
-__global__ void __launch_bounds__(gemm_threads(KS), FMT == 4 ? 3 : 2)
+__global__ void __launch_bounds__(gemm_threads(KS), FMT == 4 && KS == 1 ? 4 : 2)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap map, const GemmParams p) {
   using L = GemmLayout<FMT, NT, NSTAGE, KS>;
   constexpr int CONSUMER_WARPS = 4 * KS, THREADS = gemm_threads(KS);
