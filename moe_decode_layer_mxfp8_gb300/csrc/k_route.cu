@@ -104,35 +104,38 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-constexpr int TOPK_THREADS = 512;
+constexpr int TOPK_THREADS = 1024;
+constexpr int TOPK_BATCH = 6;  // logits per thread in flight at once
+template <int KSL>  // K slices of the router partials at most
 __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
   extern __shared__ float s_z[];  // [rows][E] logits
   __shared__ int s_idx[MAX_ROWS * MAX_K];
+  __shared__ int s_pos[MAX_ROWS];
   __shared__ unsigned long long s_mask[MAX_EXPERTS];  // rows routed to each expert
-  __shared__ int s_off[MAX_EXPERTS];
+  __shared__ int s_tot[3][MAX_EXPERTS / 32];          // per-warp totals of the expert scans
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int NW = TOPK_THREADS / 32, ZJ = MAX_EXPERTS / 32;
   for (int e = tid; e < MAX_EXPERTS; e += TOPK_THREADS) s_mask[e] = 0ull;
+  if (tid < a.rows) s_pos[tid] = a.positions[tid];  // a step input: read before the wait
   pdl_wait();
-  // phase 1a: logits = the K-slice partials summed in slice order, every load of a batch of
-  // four logits in flight at once
+  // phase 1a: logits = the K-slice partials summed in slice order
   const int nz = a.rows * a.E;
-  for (int base = tid; base < nz; base += 4 * TOPK_THREADS) {
-    float pz[4][ROUTER_MAX_KSLICES];
+  for (int base = tid; base < nz; base += TOPK_BATCH * TOPK_THREADS) {
+    float pz[TOPK_BATCH][KSL];
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < TOPK_BATCH; ++u)
 #pragma unroll
-      for (int ks = 0; ks < ROUTER_MAX_KSLICES; ++ks) {
+      for (int ks = 0; ks < KSL; ++ks) {
         const int i = base + u * TOPK_THREADS;
         pz[u][ks] = i < nz && ks < a.kslices ? a.partial[(size_t)ks * nz + i] : 0.0f;
       }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < TOPK_BATCH; ++u) {
       const int i = base + u * TOPK_THREADS;
       float z = 0.0f;
 #pragma unroll
-      for (int ks = 0; ks < ROUTER_MAX_KSLICES; ++ks)
+      for (int ks = 0; ks < KSL; ++ks)
         if (ks < a.kslices) z += pz[u][ks];
       if (i < nz) {
         s_z[i] = z;
@@ -143,7 +146,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
   __syncthreads();
   // phase 1b: selection, a warp a row
   for (int r = warp; r < a.rows; r += NW) {
-    const bool pad = a.positions[r] < 0;
+    const bool pad = s_pos[r] < 0;
     uint32_t key[ZJ];
 #pragma unroll
     for (int j = 0; j < ZJ; ++j) {
@@ -187,46 +190,51 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
     }
   }
   __syncthreads();
-  // phase 2: prefix sums over experts (one warp; E <= 256)
-  if (warp == 0) {
-    int run_off = 0, run_hit = 0, run_rg = 0;
-    for (int base = 0; base < MAX_EXPERTS; base += 32) {
-      const int e = base + lane;
-      const int c = e < a.E ? __popcll(s_mask[e]) : 0;
-      const int hit = c > 0, rg = (c + EXPERT_ROWS - 1) / EXPERT_ROWS;
-      int ic = c, ih = hit, ir = rg;
+  // phase 2: prefix sums over experts: warp w scans experts 32w..32w+31, then adds the
+  // totals of the warps before it
+  constexpr int SW = MAX_EXPERTS / 32;
+  int c = 0, hit = 0, rg = 0, ic = 0, ih = 0, ir = 0;
+  const int e = warp * 32 + lane;
+  if (warp < SW) {
+    c = e < a.E ? __popcll(s_mask[e]) : 0;
+    hit = c > 0;
+    rg = (c + EXPERT_ROWS - 1) / EXPERT_ROWS;
+    ic = c, ih = hit, ir = rg;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {  // inclusive warp scans
-        const int tc = __shfl_up_sync(0xffffffffu, ic, o);
-        const int th = __shfl_up_sync(0xffffffffu, ih, o);
-        const int tr = __shfl_up_sync(0xffffffffu, ir, o);
-        if (lane >= o) ic += tc, ih += th, ir += tr;
-      }
-      s_off[e] = run_off + ic - c;
-      if (c > 0) {
-        const int d = run_hit + ih - hit;
-        a.route->hit_e[d] = e;
-        a.route->hit_off[d] = run_off + ic - c;
-        a.route->hit_cnt[d] = c;
-        a.route->rg_prefix[d] = run_rg + ir - rg;
-      }
-      run_off += __shfl_sync(0xffffffffu, ic, 31);
-      run_hit += __shfl_sync(0xffffffffu, ih, 31);
-      run_rg += __shfl_sync(0xffffffffu, ir, 31);
+    for (int o = 1; o < 32; o <<= 1) {  // inclusive warp scans
+      const int tc = __shfl_up_sync(0xffffffffu, ic, o);
+      const int th = __shfl_up_sync(0xffffffffu, ih, o);
+      const int tr = __shfl_up_sync(0xffffffffu, ir, o);
+      if (lane >= o) ic += tc, ih += th, ir += tr;
     }
-    if (lane == 0) {
-      a.route->n_hit = run_hit;
-      a.route->rg_prefix[run_hit] = run_rg;
+    if (lane == 31) s_tot[0][warp] = ic, s_tot[1][warp] = ih, s_tot[2][warp] = ir;
+  }
+  __syncthreads();
+  __shared__ int s_off[MAX_EXPERTS];
+  if (warp < SW) {
+    int bo = 0, bh = 0, br = 0;
+    for (int w = 0; w < warp; ++w) bo += s_tot[0][w], bh += s_tot[1][w], br += s_tot[2][w];
+    const int off = bo + ic - c, d = bh + ih - hit, rgp = br + ir - rg;
+    s_off[e] = off;
+    if (c > 0) {
+      a.route->hit_e[d] = e;
+      a.route->hit_off[d] = off;
+      a.route->hit_cnt[d] = c;
+      a.route->rg_prefix[d] = rgp;
+    }
+    if (warp == SW - 1 && lane == 31) {
+      a.route->n_hit = bh + ih;
+      a.route->rg_prefix[bh + ih] = br + ir;
     }
   }
   __syncthreads();
   // phase 3: stable placement -- an expert's entries in row order (a row picks an expert once)
   const int n = a.rows * a.k;
   for (int q = tid; q < n; q += TOPK_THREADS) {
-    const int e = s_idx[q];
-    if (e >= 0) {
+    const int ex = s_idx[q];
+    if (ex >= 0) {
       const int r = q / a.k;
-      const int pos = s_off[e] + __popcll(s_mask[e] & ((1ull << r) - 1ull));
+      const int pos = s_off[ex] + __popcll(s_mask[ex] & ((1ull << r) - 1ull));
       a.slot_pos[q] = pos;
       a.perm[pos] = r;
     } else {
@@ -247,8 +255,11 @@ cudaError_t router_prepare() {
   cudaError_t e = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        router_smem_bytes(MAX_ROWS));
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              topk_smem_bytes());
+  for (auto k : {topk_kernel<1>, topk_kernel<2>, topk_kernel<4>, topk_kernel<8>}) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, topk_smem_bytes());
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_router(const Launch& L, const RouterArgs& a) {
@@ -257,7 +268,11 @@ cudaError_t launch_router(const Launch& L, const RouterArgs& a) {
 }
 
 cudaError_t launch_topk(const Launch& L, const TopkArgs& a) {
-  return launch_ex(L, dim3(1), dim3(TOPK_THREADS), a.rows * a.E * 4, topk_kernel, a);
+  const int smem = a.rows * a.E * 4;
+  if (a.kslices <= 1) return launch_ex(L, dim3(1), dim3(TOPK_THREADS), smem, topk_kernel<1>, a);
+  if (a.kslices <= 2) return launch_ex(L, dim3(1), dim3(TOPK_THREADS), smem, topk_kernel<2>, a);
+  if (a.kslices <= 4) return launch_ex(L, dim3(1), dim3(TOPK_THREADS), smem, topk_kernel<4>, a);
+  return launch_ex(L, dim3(1), dim3(TOPK_THREADS), smem, topk_kernel<8>, a);
 }
 
 }  // namespace mono

@@ -429,6 +429,11 @@ __device__ void epilogue_local(const GemmParams& p, const Item& it, float* ep, i
   store_rows<EP_LD, NTHR>(p, it, ep, 0, sw ? BOX_ROWS : TILE_M, tid);
 }
 
+// owner_epilogue with the cluster size and the SwiGLU pairing as compile-time constants.
+template <int EP_LD, int NTHR>
+__device__ __forceinline__ void owner_epilogue_any(const GemmParams& p, const Item& it,
+                                                   const float* recv, int tid, uint32_t rank);
+
 // Accumulators of consumer warp (M-tile mt) into its K share's partial tile.
 template <int NT, int EP_LD>
 __device__ __forceinline__ void write_partial(const float (&acc)[NT][4], float* ep_mine, int mt,
@@ -449,7 +454,8 @@ __device__ __forceinline__ void write_partial(const float (&acc)[NT][4], float* 
 // The K shares' partial tiles added, in a fixed order, into the first.
 template <int KS, int EP_LD, int NTHR>
 __device__ __forceinline__ void sum_kshares(float* ep, int ntl, int tid) {
-  const int cols = ntl * 8;
+  (void)ntl;
+  constexpr int cols = EP_LD - 1;  // every column of the tile (a compile-time divisor)
   for (int idx = tid; idx < TILE_M * cols; idx += NTHR) {
     const int m = idx / cols, col = idx - m * cols;
     float v = ep[m * EP_LD + col];
@@ -489,13 +495,13 @@ __device__ __forceinline__ void push_slices(const GemmParams& p, const float* pa
 
 // The owner's share of a K-split tile: adds its receive slots in slot order and writes its
 // columns out, two values per thread in flight at a time.
-template <int EP_LD, int NTHR>
+template <int EP_LD, int NTHR, int KSPLIT, bool SW>
 __device__ void owner_epilogue(const GemmParams& p, const Item& it, const float* recv, int tid,
                                uint32_t rank) {
-  const bool sw = p.epi == EPI_SWIGLU_F16;
-  const int ks = p.ksplit;
-  const int per = (sw ? BOX_ROWS : TILE_M) / ks;
-  const int srows = TILE_M / ks;
+  constexpr bool sw = SW;
+  constexpr int ks = KSPLIT;
+  constexpr int per = (SW ? BOX_ROWS : TILE_M) / KSPLIT;
+  constexpr int srows = TILE_M / KSPLIT;
   const int total = per * it.n;
   const int ncols = sw ? p.swiglu_I : p.N;
   constexpr int B = 2;
@@ -515,6 +521,7 @@ __device__ void owner_epilogue(const GemmParams& p, const Item& it, const float*
                  : 0.0f;
       float s = 0.0f, su = 0.0f;
       if (idx < total) {
+#pragma unroll
         for (int sl = 0; sl < ks; ++sl) {
           const float* q = recv + (sl * srows + lr) * EP_LD + i;
           s += q[0];
@@ -543,6 +550,24 @@ __device__ void owner_epilogue(const GemmParams& p, const Item& it, const float*
       }
     }
   }
+}
+
+template <int EP_LD, int NTHR>
+__device__ __forceinline__ void owner_epilogue_any(const GemmParams& p, const Item& it,
+                                                   const float* recv, int tid, uint32_t rank) {
+  const bool sw = p.epi == EPI_SWIGLU_F16;
+#define MONO_OWNER_CASE(K)                                                         \
+  case K:                                                                          \
+    if (sw) owner_epilogue<EP_LD, NTHR, K, true>(p, it, recv, tid, rank);          \
+    else owner_epilogue<EP_LD, NTHR, K, false>(p, it, recv, tid, rank);            \
+    break;
+  switch (p.ksplit) {
+    MONO_OWNER_CASE(2)
+    MONO_OWNER_CASE(4)
+    MONO_OWNER_CASE(8)
+    default: break;  // ksplit in {2, 4, 8} for every clustered launch (host-checked)
+  }
+#undef MONO_OWNER_CASE
 }
 
 // E8M0 byte -> 2^(e-127) for e in 1..254 by placing the byte in the f32 exponent field
@@ -706,7 +731,7 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
         push_slices<L::EP_LD>(p, ep, recv, red_full, rank, it.n);
       }
       if (!pipe_wait(red_full, tiles_done & 1, p.status, abort)) return;
-      owner_epilogue<L::EP_LD, NTHR>(p, it, recv, tid, rank);
+      owner_epilogue_any<L::EP_LD, NTHR>(p, it, recv, tid, rank);
       if (tid == 0) bulk_wait_read();  // this CTA's pushes have read its partial tile
       consumer_bar<NTHR>();
       if (tid < p.ksplit) mbar_arrive_remote(mapa_shared(smem_u32(red_done), tid));  // tile free
