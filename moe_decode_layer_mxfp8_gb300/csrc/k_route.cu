@@ -9,8 +9,8 @@
 // sum.
 //
 // topk_kernel sums the partials in slice order (a fixed order, so results replay
-// bit-exactly) into shared memory, picks the top-k per row (a warp per row: the largest key
-// by warp max-reduction, ties to the lowest expert index by a min-reduction) and sorts the
+// bit-exactly) into shared memory, picks the top-k per row (a group of 8 or 16 lanes per
+// row: the largest (logit, lowest index) by a butterfly max per round) and sorts the
 // (row, slot) pairs by expert, stably, for the grouped expert GEMMs: a row picks an expert
 // at most once, so an entry's place among its expert's entries is the number of earlier
 // rows in that expert's row mask.
@@ -104,8 +104,8 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-constexpr int TOPK_THREADS = 1024;
-constexpr int TOPK_BATCH = 6;  // logits per thread in flight at once
+constexpr int TOPK_THREADS = 512;
+constexpr int TOPK_BATCH = 12;  // logits per thread in flight at once
 template <int KSL>  // K slices of the router partials at most
 __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
   extern __shared__ float s_z[];  // [rows][E] logits
@@ -144,49 +144,57 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
     }
   }
   __syncthreads();
-  // phase 1b: selection, a warp a row
-  for (int r = warp; r < a.rows; r += NW) {
-    const bool pad = s_pos[r] < 0;
-    uint32_t key[ZJ];
+  // phase 1b: selection.  A group of LPR lanes per row (8 for E <= 128, 16 for E <= 256),
+  // 16 logits per lane packed with their expert index as (order key << 32 | 255 - e): the
+  // largest packed value is the largest logit, ties to the lowest expert index.  k rounds of
+  // a local max and a butterfly over the group.
+  {
+    const int lpr = a.E <= 128 ? 8 : 16;
+    const int rpw = 32 / lpr;  // rows per warp
+    const int li = lane & (lpr - 1), grp = lane / lpr;
+    for (int r0 = warp * rpw; r0 < a.rows; r0 += NW * rpw) {
+      const int r = r0 + grp;
+      const bool live = r < a.rows;
+      unsigned long long pv[16];
 #pragma unroll
-    for (int j = 0; j < ZJ; ++j) {
-      const int e = lane + 32 * j;
-      key[j] = e < a.E ? order_key(s_z[r * a.E + e] + 0.0f) : 0u;  // (-0 -> +0); 0: below all
-    }
-    // k rounds of: largest key over the warp, then the lowest expert index holding it
-    float zsel0 = 0.0f, ex_sum = 0.0f, my_ex = 0.0f;
-    int my_e = -1;
-#pragma unroll
-    for (int kk = 0; kk < MAX_K; ++kk) {
-      if (kk < a.k) {
-        uint32_t lk = 0u;
-#pragma unroll
-        for (int j = 0; j < ZJ; ++j) lk = max(lk, key[j]);
-        const uint32_t mk = __reduce_max_sync(0xffffffffu, lk);
-        uint32_t cand = 0xffffffffu;
-#pragma unroll
-        for (int j = ZJ - 1; j >= 0; --j)
-          if (key[j] == mk) cand = lane + 32 * j;
-        const int be = (int)__reduce_min_sync(0xffffffffu, cand);
-        const float bv = key_value(mk);
-        if (kk == 0) zsel0 = bv;
-        const float ex = expf(bv - zsel0);
-        ex_sum += ex;
-        if (lane == kk) my_ex = ex, my_e = be;  // lane kk keeps slot kk
-#pragma unroll
-        for (int j = 0; j < ZJ; ++j)
-          if (lane + 32 * j == be) key[j] = 0u;
+      for (int j = 0; j < 16; ++j) {
+        const int e = li + lpr * j;
+        pv[j] = live && e < a.E
+                    ? ((unsigned long long)order_key(s_z[r * a.E + e] + 0.0f) << 32) |
+                          (unsigned long long)(255 - e)
+                    : 0ull;  // (-0 -> +0 above); 0 sorts below every logit
       }
-    }
-    if (lane < a.k) {
-      const int e = pad ? -1 : my_e;
-      const float wgt = pad ? 0.0f : my_ex / ex_sum * a.routed_scale;
-      s_idx[r * a.k + lane] = e;
-      a.topk_idx[r * a.k + lane] = e;
-      a.topk_w[r * a.k + lane] = wgt;
-      if (a.user_idx) a.user_idx[r * a.k + lane] = e;
-      if (a.user_w) a.user_w[r * a.k + lane] = wgt;
-      if (e >= 0) atomicOr(&s_mask[e], 1ull << r);
+      float zsel0 = 0.0f, ex_sum = 0.0f, my_ex = 0.0f;
+      int my_e = -1;
+#pragma unroll
+      for (int kk = 0; kk < MAX_K; ++kk) {
+        if (kk < a.k) {
+          unsigned long long b = 0ull;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) b = max(b, pv[j]);
+          for (int o = 1; o < lpr; o <<= 1) b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
+          const int be = 255 - (int)(b & 0xFFull);
+          const float bv = key_value((uint32_t)(b >> 32));
+          if (kk == 0) zsel0 = bv;
+          const float ex = expf(bv - zsel0);
+          ex_sum += ex;
+          if (li == kk) my_ex = ex, my_e = be;  // lane kk of the group keeps slot kk
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (li + lpr * j == be) pv[j] = 0ull;
+        }
+      }
+      if (live && li < a.k) {
+        const bool pad = s_pos[r] < 0;
+        const int e = pad ? -1 : my_e;
+        const float wgt = pad ? 0.0f : my_ex / ex_sum * a.routed_scale;
+        s_idx[r * a.k + li] = e;
+        a.topk_idx[r * a.k + li] = e;
+        a.topk_w[r * a.k + li] = wgt;
+        if (a.user_idx) a.user_idx[r * a.k + li] = e;
+        if (a.user_w) a.user_w[r * a.k + li] = wgt;
+        if (e >= 0) atomicOr(&s_mask[e], 1ull << r);
+      }
     }
   }
   __syncthreads();
