@@ -1,8 +1,8 @@
 // Router and expert grouping ("Mono decode layer for DeepSeek-V4.1-Flash on MI355X", launch
 // table K2: "router, top-6"; ATOM changes: "f32 router logits").
 //
-// router_kernel: z[r, e] = u[r] . W_r[e] in f32, split over K: CTA (4 experts, 1024-wide K
-// slice) holds its experts' weight slices in registers (fetched before waiting on the
+// router_kernel: z[r, e] = u[r] . W_r[e] in f32, split over K: CTA (4 experts x 2 warps,
+// 1024-wide K slice) holds its experts' weight slices in registers (fetched before waiting on the
 // previous kernel), stages the slice of every row of u in shared memory and writes one
 // partial per (slice, row, expert).  Rows go eight at a time: eight independent FMA chains
 // per lane, then one transposing butterfly that leaves each of eight lanes with one row's
@@ -20,8 +20,9 @@ namespace mono {
 
 namespace {
 
-constexpr int RT_EXPERTS = 4;    // experts per CTA, one warp each
-constexpr int RT_THREADS = RT_EXPERTS * 32;
+constexpr int RT_EXPERTS = 4;    // experts per CTA
+constexpr int RT_HALVES = 2;     // warps per expert, taking alternate groups of 8 rows
+constexpr int RT_THREADS = RT_EXPERTS * RT_HALVES * 32;
 constexpr int RT_J = ROUTER_KSLICE / 128;  // float4 weight chunks per lane
 constexpr int MAX_ROWS = 48, MAX_K = 8;
 
@@ -33,7 +34,8 @@ __global__ void __launch_bounds__(RT_THREADS) router_kernel(RouterArgs a) {
   const int k0 = blockIdx.y * ROUTER_KSLICE;
   const int klen = min(ROUTER_KSLICE, a.H - k0);
   // this lane's weights (k = k0 + 128 j + 4 lane + {0..3}): constant, so fetched first
-  const int e = blockIdx.x * RT_EXPERTS + warp;
+  const int e = blockIdx.x * RT_EXPERTS + (warp % RT_EXPERTS);
+  const int half = warp / RT_EXPERTS;
   float4 wv[RT_J];
 #pragma unroll
   for (int j = 0; j < RT_J; ++j)
@@ -51,24 +53,28 @@ __global__ void __launch_bounds__(RT_THREADS) router_kernel(RouterArgs a) {
   if (e >= a.E) return;
   // lane l ends a group of eight rows with the sum of row 4 bit4(l) + 2 bit3(l) + bit2(l)
   const int my_row = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-  for (int r0 = 0; r0 < a.rows; r0 += 8) {
+  for (int r0 = 8 * half; r0 < a.rows; r0 += 8 * RT_HALVES) {
     float acc[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      acc[i] = 0.0f;
-      if (r0 + i < a.rows) {
-        const __half* ur = us + (r0 + i) * ROUTER_KSLICE + 4 * lane;
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+    const int nr = min(8, a.rows - r0);
 #pragma unroll
-        for (int j = 0; j < RT_J; ++j) {
-          if (128 * j < klen) {
-            const uint2 uv = lds64(ur + 128 * j);
-            const float2 u0 = __half22float2(*reinterpret_cast<const __half2*>(&uv.x));
-            const float2 u1 = __half22float2(*reinterpret_cast<const __half2*>(&uv.y));
-            acc[i] = fmaf(u0.x, wv[j].x, acc[i]);
-            acc[i] = fmaf(u0.y, wv[j].y, acc[i]);
-            acc[i] = fmaf(u1.x, wv[j].z, acc[i]);
-            acc[i] = fmaf(u1.y, wv[j].w, acc[i]);
-          }
+    for (int j = 0; j < RT_J; ++j) {
+      if (128 * j < klen) {
+        // the eight rows' values of this chunk first, then eight independent FMA chains
+        uint2 uv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          uv[i] = i < nr ? *reinterpret_cast<const uint2*>(us + (r0 + i) * ROUTER_KSLICE + 128 * j + 4 * lane)
+                         : make_uint2(0u, 0u);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 u0 = __half22float2(*reinterpret_cast<const __half2*>(&uv[i].x));
+          const float2 u1 = __half22float2(*reinterpret_cast<const __half2*>(&uv[i].y));
+          acc[i] = fmaf(u0.x, wv[j].x, acc[i]);
+          acc[i] = fmaf(u0.y, wv[j].y, acc[i]);
+          acc[i] = fmaf(u1.x, wv[j].z, acc[i]);
+          acc[i] = fmaf(u1.y, wv[j].w, acc[i]);
         }
       }
     }
