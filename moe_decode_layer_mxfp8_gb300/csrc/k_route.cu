@@ -110,8 +110,50 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
+struct Pick {
+  int e;      // expert of slot li of the row (lanes li < k)
+  float ex;   // its exp(z - z_max)
+  float sum;  // the sum of exp(z - z_max) over the row's k picks
+};
+
+// Top-k of one row of logits by a group of lpr lanes (8 for E <= 128, 16 for E <= 256), 16
+// logits per lane packed with their expert index as (order key << 32 | 255 - e): the
+// largest packed value is the largest logit, ties to the lowest expert index; k rounds of a
+// local max and a butterfly over the group.  Not inlined, so that the kernel's call before
+// griddepcontrol.wait (on no data, with live false) brings exactly this code into the
+// instruction caches: the kernel runs once per step and its code is otherwise cold.
+__device__ __noinline__ Pick select_topk(const float* z, int E, int k, int lpr, int li, bool live) {
+  unsigned long long pv[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int e = li + lpr * j;
+    pv[j] = live && e < E ? ((unsigned long long)order_key(z[e] + 0.0f) << 32) |
+                                (unsigned long long)(255 - e)
+                          : 0ull;  // (-0 -> +0 above); 0 sorts below every logit
+  }
+  Pick pk = {-1, 0.0f, 0.0f};
+  float zsel0 = 0.0f;
+#pragma unroll 1
+  for (int kk = 0; kk < k; ++kk) {
+    unsigned long long b = 0ull;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) b = max(b, pv[j]);
+    for (int o = 1; o < lpr; o <<= 1) b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
+    const int be = 255 - (int)(b & 0xFFull);
+    const float bv = key_value((uint32_t)(b >> 32));
+    if (kk == 0) zsel0 = bv;
+    const float ex = expf(bv - zsel0);
+    pk.sum += ex;
+    if (li == kk) pk.ex = ex, pk.e = be;  // lane kk of the group keeps slot kk
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (li + lpr * j == be) pv[j] = 0ull;
+  }
+  return pk;
+}
+
 constexpr int TOPK_THREADS = 512;
-constexpr int TOPK_BATCH = 12;  // logits per thread in flight at once
+constexpr int TOPK_BATCH = 4;  // logits per thread in flight at once
 template <int KSL>  // K slices of the router partials at most
 __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
   extern __shared__ float s_z[];  // [rows][E] logits
@@ -124,6 +166,10 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
   constexpr int NW = TOPK_THREADS / 32, ZJ = MAX_EXPERTS / 32;
   for (int e = tid; e < MAX_EXPERTS; e += TOPK_THREADS) s_mask[e] = 0ull;
   if (tid < a.rows) s_pos[tid] = a.positions[tid];  // a step input: read before the wait
+  if (warp == 0) {  // warm the selection code while the previous kernel finishes
+    const Pick dry = select_topk(s_z, a.E, a.k, a.E <= 128 ? 8 : 16, lane & 7, false);
+    if (dry.e == -2) s_pos[0] = 0;  // never true: keeps the call
+  }
   pdl_wait();
   // phase 1a: logits = the K-slice partials summed in slice order
   const int nz = a.rows * a.E;
@@ -150,10 +196,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
     }
   }
   __syncthreads();
-  // phase 1b: selection.  A group of LPR lanes per row (8 for E <= 128, 16 for E <= 256),
-  // 16 logits per lane packed with their expert index as (order key << 32 | 255 - e): the
-  // largest packed value is the largest logit, ties to the lowest expert index.  k rounds of
-  // a local max and a butterfly over the group.
+  // phase 1b: selection, a group of 8 or 16 lanes per row (select_topk)
   {
     const int lpr = a.E <= 128 ? 8 : 16;
     const int rpw = 32 / lpr;  // rows per warp
@@ -161,35 +204,9 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
     for (int r0 = warp * rpw; r0 < a.rows; r0 += NW * rpw) {
       const int r = r0 + grp;
       const bool live = r < a.rows;
-      unsigned long long pv[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int e = li + lpr * j;
-        pv[j] = live && e < a.E
-                    ? ((unsigned long long)order_key(s_z[r * a.E + e] + 0.0f) << 32) |
-                          (unsigned long long)(255 - e)
-                    : 0ull;  // (-0 -> +0 above); 0 sorts below every logit
-      }
-      float zsel0 = 0.0f, ex_sum = 0.0f, my_ex = 0.0f;
-      int my_e = -1;
-#pragma unroll
-      for (int kk = 0; kk < MAX_K; ++kk) {
-        if (kk < a.k) {
-          unsigned long long b = 0ull;
-#pragma unroll
-          for (int j = 0; j < 16; ++j) b = max(b, pv[j]);
-          for (int o = 1; o < lpr; o <<= 1) b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
-          const int be = 255 - (int)(b & 0xFFull);
-          const float bv = key_value((uint32_t)(b >> 32));
-          if (kk == 0) zsel0 = bv;
-          const float ex = expf(bv - zsel0);
-          ex_sum += ex;
-          if (li == kk) my_ex = ex, my_e = be;  // lane kk of the group keeps slot kk
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (li + lpr * j == be) pv[j] = 0ull;
-        }
-      }
+      const Pick pk = select_topk(s_z + r * a.E, a.E, a.k, lpr, li, live);
+      const int my_e = pk.e;
+      const float my_ex = pk.ex, ex_sum = pk.sum;
       if (live && li < a.k) {
         const bool pad = s_pos[r] < 0;
         const int e = pad ? -1 : my_e;
@@ -261,7 +278,12 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
 
 int router_smem_bytes(int rows) { return rows * ROUTER_KSLICE * 2; }
 // The logits of the step in shared memory, [rows][E].
-int topk_smem_bytes() { return MAX_ROWS * MAX_EXPERTS * 4; }
+// The kernel is one latency-bound CTA: it asks for more shared memory than its logits need
+// (200 KB) so that no GEMM CTA of the concurrently running shared expert lands on its SM and
+// competes for its issue slots.
+constexpr int TOPK_SMEM = 200 * 1024;
+static_assert(TOPK_SMEM >= MAX_ROWS * MAX_EXPERTS * 4, "the logits must fit");
+int topk_smem_bytes() { return TOPK_SMEM; }
 
 // The limits are properties of the kernels, shared by every layer handle of the process: set
 // them for the largest step any handle accepts.
@@ -282,7 +304,7 @@ cudaError_t launch_router(const Launch& L, const RouterArgs& a) {
 }
 
 cudaError_t launch_topk(const Launch& L, const TopkArgs& a) {
-  const int smem = a.rows * a.E * 4;
+  const int smem = TOPK_SMEM;
   if (a.kslices <= 1) return launch_ex(L, dim3(1), dim3(TOPK_THREADS), smem, topk_kernel<1>, a);
   if (a.kslices <= 2) return launch_ex(L, dim3(1), dim3(TOPK_THREADS), smem, topk_kernel<2>, a);
   if (a.kslices <= 4) return launch_ex(L, dim3(1), dim3(TOPK_THREADS), smem, topk_kernel<4>, a);
