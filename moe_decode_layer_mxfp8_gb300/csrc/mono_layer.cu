@@ -521,8 +521,8 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
   RUN(launch_router(L, {h->buf<__half>(MONO_BUF_U), h->w.router, R, E, H, h->router_part}));
   // The shared expert depends only on u: fork it onto the side stream after the router (whose
   // CTAs are then resident before the shared expert's GEMM CTAs claim the SMs) so that it
-  // overlaps the top-k; the routed experts start once both branches are done.  While
-  // profiling, everything stays on one stream in launch-name order.
+  // overlaps the top-k (and, in large steps, the routed experts).  While profiling,
+  // everything stays on one stream in launch-name order.
   const bool fork = !h->profiling;
   const Launch Ls{fork ? h->side : stream, !h->profiling};
   if (fork) {
@@ -561,9 +561,13 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     t.status = h->status;
     RUN(launch_topk(L, t));
   }
-  if (fork) {
+  // Large steps: the persistent expert GEMM starts right after the top-k and the shared
+  // expert joins before the final combine.  Small steps: the routed experts' clusters want
+  // every SM at once (items are assigned statically), so they wait for the shared expert.
+  const bool late_join = fork && R * K > EXPERT_SMALL_SLOTS;
+  if (fork && !late_join) {
     RUN_PLAIN(cudaStreamWaitEvent(stream, h->ev_join, 0));
-  } else {
+  } else if (!fork) {
     const int rs = shared_expert();
     if (rs != MONO_OK) return rs;
   }
@@ -572,6 +576,7 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
              s.moe_inter));
   RUN(expert(h->map_ex_d, h->w.ex_d_s, s.moe_inter, H, 0, H / TILE_M, h->buf<__half>(MONO_BUF_TR),
              s.moe_inter, nullptr, EPI_F32, h->buf<void>(MONO_BUF_YR), H));
+  if (late_join) RUN_PLAIN(cudaStreamWaitEvent(stream, h->ev_join, 0));
   {
     FinalArgs f = {};
     f.x = x;
