@@ -374,9 +374,9 @@ def _workload_desc(name, spec, rows):
 # kernel, from the ncu capture summarised in profiles/expert_gate_up_full_r48.md, keyed by
 # the md5 of the GEMM sources it was taken on: reported only while those are unchanged.
 NCU_TRAFFIC = {
-    ("full_r48", "expert_gate_up"): (499_417_088, "35ab6c4540fb050b076769dea45c17b0"
-                                                  "d8cc55517e409104957990358e50ec40"
-                                                  "0d5ea4d34680824b9da5edc280a0c7a8"),
+    ("full_r48", "expert_gate_up"): (499_536_896, "2c836b62a75295056467863cd042bb8c"
+                                                  "efa9de8d5a3faafd2b3661cb52529d55"
+                                                  "f4a1d65a57a56dec41dc2f07972e1b1a"),
 }
 
 
