@@ -58,6 +58,19 @@ WORKLOADS = {
                      rows_per_req=6, pad_rows=0, seed=2, repeat_input=True),
     "full_r48": dict(spec=_FULL, contexts="uniform:1024:65536:8", rows_per_req=6,
                      pad_rows=0, seed=3),
+    # parity-only shapes that reach the remaining code paths: 4 one-token requests (a small
+    # step whose many expert items do not split K), 24 rows (the 4-tile dense variant), and a
+    # narrow layer with 256 experts, top-8, head_dim 64 and a 300-token window (3 splits)
+    "full_r4": dict(spec=_FULL, contexts=[3000, 70, 20000, 129], rows_per_req=1, pad_rows=0,
+                    seed=11),
+    "full_r24": dict(spec=_FULL, contexts="uniform:1024:65536:4", rows_per_req=6, pad_rows=0,
+                     seed=12),
+    "wide_r9": dict(spec=dict(hidden=1024, n_q_heads=16, head_dim=64, kv_dim=128, q_rank=256,
+                              o_rank=256, n_experts=256, topk=8, moe_inter=256,
+                              shared_inter=512, window=300, swa_width=300, causal=1,
+                              block_size=64, kv_record_bytes=144, eps=1e-6, swiglu_clamp=7.0,
+                              routed_scale=2.5),
+                    contexts=[400, 350, 900], rows_per_req=[3, 3, 2], pad_rows=1, seed=13),
 }
 
 

@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
   __shared__ int s_tot[3][MAX_EXPERTS / 32];          // per-warp totals of the expert scans
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr int NW = TOPK_THREADS / 32, ZJ = MAX_EXPERTS / 32;
+  constexpr int NW = TOPK_THREADS / 32;
   for (int e = tid; e < MAX_EXPERTS; e += TOPK_THREADS) s_mask[e] = 0ull;
   if (tid < a.rows) s_pos[tid] = a.positions[tid];  // a step input: read before the wait
   if (warp == 0) {  // warm the selection code while the previous kernel finishes
