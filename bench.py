@@ -4,7 +4,9 @@ bandwidth it sustains, on synthetic seeded inputs.
 Headline workload: one full-size layer at 48 rows (8 requests x 6 rows, causal window 128,
 contexts uniform in [1024, 65536], 128 experts top-6), the configuration the 60%-of-HBM
 target is set on.  The same JSON line carries the 1-row and 6-row (draft, top-3,
-non-causal 192-wide rows) shapes under "rows_sweep".
+non-causal 192-wide rows) shapes under "rows_sweep", together with the stacked decode step
+(30 full-size 48-row layers with distinct weights and KV caches, each layer's output the
+next one's input, one CUDA graph: "stacked_30x48").
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -233,6 +235,63 @@ def measure_device(name, steps, warmup, dev, n_copies, sampler=None):
                bytes=avg_bytes, bytes_detail=byte_list[0], d_hit=[b["d_hit"] for b in byte_list],
                launches=steps * layers[0][0].launches_per_step(), copies=C)
     return res
+
+
+STACKED_LAYERS = 30
+
+
+def measure_stacked(n_layers, steps, warmup, dev):
+    """The stacked decode step: n_layers full-size 48-row layers with distinct weights and
+    KV caches, each layer's output the next one's input, captured as one CUDA graph.
+    Returns us per stacked step and the algorithmic bytes it touches."""
+    import moe_decode_layer_mxfp8_gb300 as m
+    name = "full_r48"
+    wl = gen.WORKLOADS[name]
+    spec = gen.spec_of(name)
+    step = gen.make_step(spec, wl, device=dev)
+    spec["max_rows"] = step["rows"]
+    caches = [step["kv_cache"]] + [step["kv_cache"].clone() for _ in range(n_layers - 1)]
+    layers = [m.Layer(spec, gen.make_weights(spec, wl["seed"] + 1000 * (c + 7), device=dev))
+              for c in range(n_layers)]
+    xs = [step["x"].clone(), torch.empty_like(step["x"])]
+    stream = torch.cuda.Stream(dev)
+    idx = torch.empty((step["rows"], spec["topk"]), dtype=torch.int32, device=dev)
+    total = 0.0
+    d_hit = []
+    with torch.cuda.stream(stream):
+        for i, lay in enumerate(layers):  # eager once: routing of every layer, for its bytes
+            lay.step(xs[i % 2], xs[(i + 1) % 2], step["positions"], step["row_req"],
+                     step["block_table"], caches[i], stream=stream, topk_idx_out=idx)
+            stream.synchronize()
+            b = step_bytes(spec, step, idx.cpu().numpy())
+            total += b["total"]
+            d_hit.append(b["d_hit"])
+        for lay in layers:
+            assert lay.status() == 0
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i, lay in enumerate(layers):
+                lay.step(xs[i % 2], xs[(i + 1) % 2], step["positions"], step["row_req"],
+                         step["block_table"], caches[i], stream=stream)
+        for _ in range(max(3, warmup)):
+            g.replay()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        t1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = t0.elapsed_time(t1) * 1000.0 / steps
+    for lay in layers:
+        lay.close()
+    del layers, caches, g
+    torch.cuda.empty_cache()
+    return dict(layers=n_layers, rows=step["rows"], us_per_step=round(us, 1),
+                us_per_layer=round(us / n_layers, 2), bytes_per_step=int(total),
+                hbm_gbs=round(total / us / 1e3, 1),
+                frac_of_measured_copy=None, d_hit_min=int(min(d_hit)), d_hit_max=int(max(d_hit)))
 
 
 def kernel_profile(res, dev, reps=20):
@@ -473,6 +532,10 @@ def main():
                                    bytes_per_step=int(r["bytes"]), d_hit=r["d_hit"])
                 del r
                 torch.cuda.empty_cache()
+            # configuration 5: 30 stacked 48-row layers, one graph, residual carried
+            stacked = measure_stacked(STACKED_LAYERS, 20, args.warmup, dev)
+            stacked["frac_of_measured_copy"] = round(stacked["hbm_gbs"] / peak, 4)
+            sweep["stacked_30x48"] = stacked
     clocks = clk.summary()
 
     prof = kernel_profile(res, dev)
