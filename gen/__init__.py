@@ -269,6 +269,16 @@ def make_workload(name: str, device="cpu", seed: int | None = None, weight_devic
     return spec, weights, step
 
 
+def make_attn_out(spec: dict, step: dict, seed: int = 0, std: float = 0.5, device=None):
+    """The attention block's output for every row of a step, as the FFN launch takes it
+    (bf16 [rows, H]): an independent normal draw of standard deviation ``std``, on the
+    step's device unless ``device`` is given."""
+    rows, H = step["rows"], spec["hidden"]
+    g = _gen(seed * 7919 + 17, torch.device("cpu"))
+    a = torch.randn((rows, H), generator=g) * std
+    return a.to(torch.bfloat16).to(device or step["x"].device)
+
+
 def weight_bytes(spec: dict) -> dict:
     """Bytes of each weight group of one layer, as stored."""
     H, nq, dh, kv = spec["hidden"], spec["n_q_heads"], spec["head_dim"], spec["kv_dim"]
@@ -289,4 +299,4 @@ def weight_bytes(spec: dict) -> dict:
 
 
 __all__ = ["WORKLOADS", "spec_of", "make_weights", "make_step", "make_workload", "pack_mxfp8",
-           "pack_mxfp4", "weight_bytes", "WEIGHT_KEYS"]
+           "pack_mxfp4", "weight_bytes", "WEIGHT_KEYS", "make_attn_out"]

@@ -96,6 +96,10 @@ def lib():
             L.orc_layer.restype = C.c_int
             L.orc_layer.argtypes = [C.POINTER(Spec), C.POINTER(Weights), C.POINTER(Step),
                                     C.POINTER(Trace)]
+            L.orc_ffn_layer.restype = None
+            L.orc_ffn_layer.argtypes = [C.POINTER(Spec), C.POINTER(Weights), C.c_void_p,
+                                        C.c_void_p, C.c_void_p, C.c_void_p, C.c_int,
+                                        C.POINTER(Trace)]
             L.orc_kv_insert.restype = C.c_int
             L.orc_attention.restype = C.c_int
             L.orc_key_range.restype = C.c_int
@@ -315,7 +319,37 @@ def layer(spec: dict, weights: dict, step: dict, force_idx=None):
     return out
 
 
+_FFN_TKEYS = ["h", "u", "logits", "probs", "topk_idx", "topk_w", "t_s", "y_s", "t_r", "y_r",
+              "out"]
+
+
+def ffn_layer(spec: dict, weights: dict, x, attn, positions, force_idx=None):
+    """The FFN launch: the residual h = bf16(x + attn) of one step's rows, then the FFN seam
+    and the MoE (orc_ffn_layer).  x and attn are bf16 bits [rows, H]; only the FFN entries
+    of ``weights`` are read (the attention ones may be absent).  Returns a dict with h, u,
+    the routing, the expert outputs and ``out``."""
+    x, attn = _c(x, np.uint16), _c(attn, np.uint16)
+    pos = _c(positions, np.int32)
+    R = x.shape[0]
+    E, K, H = spec["n_experts"], spec["topk"], spec["hidden"]
+    I, Is = spec["moe_inter"], spec["shared_inter"]
+    dt = {"logits": np.float32, "probs": np.float64, "topk_idx": np.int32, "topk_w": np.float64,
+          "y_s": np.float64, "y_r": np.float64}
+    shapes = dict(h=(R, H), u=(R, H), logits=(R, E), probs=(R, E), topk_idx=(R, K),
+                  topk_w=(R, K), t_s=(R, Is), y_s=(R, H), t_r=(R, K, I), y_r=(R, H), out=(R, H))
+    out = {k: np.zeros(shapes[k], dt.get(k, np.uint16)) for k in _FFN_TKEYS}
+    tr = Trace(**{k: _p(out[k]) for k in _FFN_TKEYS})
+    keys = [k for k in _WKEYS if k in weights]
+    wa = {k: _c(weights[k], np.float32 if k == "router" else
+                (np.uint16 if k.endswith("norm") else np.uint8)) for k in keys}
+    w = Weights(**{k: _p(wa[k]) for k in keys})
+    fi = _c(force_idx, np.int32) if force_idx is not None else None
+    lib().orc_ffn_layer(C.byref(make_spec(spec)), C.byref(w), _p(x), _p(attn), _p(pos),
+                        _p(fi) if fi is not None else None, R, C.byref(tr))
+    return out
+
+
 __all__ = ["build", "lib", "set_threads", "get_threads", "e8m0", "e4m3", "e2m1", "encode_e4m3",
            "round_bf16", "bf16_bits", "bf16_round_array", "bf16_to_f64", "swiglu", "rmsnorm", "gemv_mxfp8",
            "gemv_mxfp4", "kv_quant", "attend", "router", "ffn", "key_range", "kv_insert",
-           "attention", "layer"]
+           "attention", "layer", "ffn_layer"]

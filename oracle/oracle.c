@@ -421,39 +421,18 @@ static void round_rows(const double *v, size_t n, uint16_t *out) {
   for (size_t i = 0; i < n; i++) out[i] = orc_bf16_bits(v[i]);
 }
 
-/* The whole layer step, stage by stage in launch order (launch table, rows K1 and K2):
- *   A1 xn = rmsnorm(x, attn_norm)                          -> bf16
- *   A2 qkv = xn . wqkv^T  (q latent of q_rank, then kv of kv_dim) -> bf16
- *   A3 q_latn = rmsnorm(q latent, q_norm); kvn = rmsnorm(kv, kv_norm) -> bf16
- *   A4 KV insert of kvn at each row's position
- *   A5 q = q_latn . wq_b^T                                  -> bf16 [rows, n_q * head_dim]
- *   B1-B2 o = windowed attention over the cache            -> bf16
- *   B3 oa = o . wo_a^T                                      -> bf16
- *   B4 h = x + oa . wo_b^T                                  -> bf16
+/* The FFN seam and the MoE of one step (launch table, row K2 from "the FFN seam" on; the
+ * same half is the whole of the row FFN), given the residual h after attention:
  *   B5 u = rmsnorm(h, ffn_norm)                             -> bf16
  *   B6 router + top-k on u
  *   B8 shared expert on u;  B9 routed experts on u, weighted
  *   B10 out = h + y_shared + sum_j w_j y_j                  -> bf16; pad rows: out = x
- * Rounding to bf16 happens exactly at the arrows; everything between is unrounded.
- * Returns 0, or -1 on a bad cache view / unmapped page. */
-int orc_layer(const orc_spec *sp, const orc_weights *w, const orc_step *st, orc_trace *tr) {
-  int R = st->rows, H = sp->hidden, qr = sp->q_rank, kvd = sp->kv_dim, orank = sp->o_rank;
-  int QW = sp->n_q_heads * sp->head_dim, E = sp->n_experts, K = sp->topk;
-  int I = sp->moe_inter, Is = sp->shared_inter, A = qr + kvd;
-  int rc = 0;
-  if (check_cache_view(sp, st)) return -1;
-
-  uint16_t *xn = malloc((size_t)R * H * 2), *qkv = malloc((size_t)R * A * 2);
-  uint16_t *qlat = malloc((size_t)R * qr * 2), *kv = malloc((size_t)R * kvd * 2);
-  uint16_t *qlatn = malloc((size_t)R * qr * 2), *kvn = malloc((size_t)R * kvd * 2);
-  uint16_t *q = malloc((size_t)R * QW * 2), *o = malloc((size_t)R * QW * 2);
-  uint16_t *oa = malloc((size_t)R * orank * 2), *h = malloc((size_t)R * H * 2);
+ * Writes out[rows, H] and the trace fields u .. y_r. */
+static void moe_half(const orc_spec *sp, const orc_weights *w, const uint16_t *x,
+                     const int32_t *positions, const int32_t *force_idx, int R,
+                     const uint16_t *h, uint16_t *out, orc_trace *tr) {
+  int H = sp->hidden, E = sp->n_experts, K = sp->topk, I = sp->moe_inter, Is = sp->shared_inter;
   uint16_t *u = malloc((size_t)R * H * 2), *ts = malloc((size_t)R * Is * 2);
-  int maxw = A;
-  if (QW > maxw) maxw = QW;
-  if (H > maxw) maxw = H;
-  if (orank > maxw) maxw = orank;
-  double *f = malloc((size_t)R * maxw * sizeof(double));
   double *ys = malloc((size_t)R * H * sizeof(double));
   double *yr = calloc((size_t)R * H, sizeof(double));
   float *logits = malloc((size_t)R * E * sizeof(float));
@@ -461,29 +440,9 @@ int orc_layer(const orc_spec *sp, const orc_weights *w, const orc_step *st, orc_
   int32_t *idx = malloc((size_t)R * K * sizeof(int32_t));
   double *wt = malloc((size_t)R * K * sizeof(double));
 
-  /* K1: attention front */
-  orc_rmsnorm(st->x, w->attn_norm, R, H, sp->eps, xn);                         /* A1 */
-  orc_gemv_mxfp8(xn, R, w->wqkv, w->wqkv_s, A, H, f);                          /* A2 */
-  round_rows(f, (size_t)R * A, qkv);
-  for (int r = 0; r < R; r++) {
-    memcpy(qlat + (size_t)r * qr, qkv + (size_t)r * A, (size_t)qr * 2);
-    memcpy(kv + (size_t)r * kvd, qkv + (size_t)r * A + qr, (size_t)kvd * 2);
-  }
-  orc_rmsnorm(qlat, w->q_norm, R, qr, sp->eps, qlatn);                         /* A3 */
-  orc_rmsnorm(kv, w->kv_norm, R, kvd, sp->eps, kvn);
-  if (orc_kv_insert(sp, st, kvn)) rc = -1;                                     /* A4 */
-  orc_gemv_mxfp8(qlatn, R, w->wq_b, w->wq_b_s, QW, qr, f);                     /* A5 */
-  round_rows(f, (size_t)R * QW, q);
-
-  /* K2: attention back, FFN seam, MoE */
-  if (orc_attention(sp, st, q, o)) rc = -1;                                    /* B1-B2 */
-  orc_gemv_mxfp8(o, R, w->wo_a, w->wo_a_s, orank, QW, f);                      /* B3 */
-  round_rows(f, (size_t)R * orank, oa);
-  orc_gemv_mxfp8(oa, R, w->wo_b, w->wo_b_s, H, orank, f);                      /* B4 */
-  for (size_t i = 0; i < (size_t)R * H; i++) h[i] = orc_bf16_bits(orc_bf16_value(st->x[i]) + f[i]);
   orc_rmsnorm(h, w->ffn_norm, R, H, sp->eps, u);                               /* B5 */
-  orc_router(u, w->router, R, E, H, K, sp->routed_scale, st->positions, st->force_idx,
-             logits, probs, idx, wt);                                          /* B6 */
+  orc_router(u, w->router, R, E, H, K, sp->routed_scale, positions, force_idx, logits, probs,
+             idx, wt);                                                         /* B6 */
   orc_ffn(u, R, 0, w->sh_gu, w->sh_gu_s, w->sh_d, w->sh_d_s, Is, H, sp->swiglu_clamp, ts,
           ys);                                                                 /* B8 */
   /* B9: each expert once, on the rows routed to it; the weighted outputs are added per row
@@ -518,13 +477,79 @@ int orc_layer(const orc_spec *sp, const orc_weights *w, const orc_step *st, orc_
         yr[(size_t)r * H + i] += wt[(size_t)r * K + j] * yslot[((size_t)r * K + j) * H + i];
     }
   /* B10 */
-  uint16_t *out = tr && tr->out ? tr->out : malloc((size_t)R * H * 2);
   for (int r = 0; r < R; r++)
     for (int i = 0; i < H; i++) {
       size_t a = (size_t)r * H + i;
-      out[a] = st->positions[r] < 0 ? st->x[a]
-                                    : orc_bf16_bits(orc_bf16_value(h[a]) + ys[a] + yr[a]);
+      out[a] = positions[r] < 0 ? x[a] : orc_bf16_bits(orc_bf16_value(h[a]) + ys[a] + yr[a]);
     }
+
+  if (tr) {
+#define KEEP(dst, src, n) if (tr->dst) memcpy(tr->dst, src, n)
+    KEEP(u, u, (size_t)R * H * 2);
+    KEEP(logits, logits, (size_t)R * E * sizeof(float));
+    KEEP(probs, probs, (size_t)R * E * sizeof(double));
+    KEEP(topk_idx, idx, (size_t)R * K * sizeof(int32_t));
+    KEEP(topk_w, wt, (size_t)R * K * sizeof(double));
+    KEEP(t_s, ts, (size_t)R * Is * 2);
+    KEEP(y_s, ys, (size_t)R * H * sizeof(double));
+    KEEP(y_r, yr, (size_t)R * H * sizeof(double));
+#undef KEEP
+  }
+  free(u), free(ts), free(ys), free(yr), free(logits), free(probs), free(idx), free(wt);
+  free(yslot), free(xe), free(te), free(yo), free(who);
+}
+
+/* The whole layer step, stage by stage in launch order (launch table, rows K1 and K2):
+ *   A1 xn = rmsnorm(x, attn_norm)                          -> bf16
+ *   A2 qkv = xn . wqkv^T  (q latent of q_rank, then kv of kv_dim) -> bf16
+ *   A3 q_latn = rmsnorm(q latent, q_norm); kvn = rmsnorm(kv, kv_norm) -> bf16
+ *   A4 KV insert of kvn at each row's position
+ *   A5 q = q_latn . wq_b^T                                  -> bf16 [rows, n_q * head_dim]
+ *   B1-B2 o = windowed attention over the cache            -> bf16
+ *   B3 oa = o . wo_a^T                                      -> bf16
+ *   B4 h = x + oa . wo_b^T                                  -> bf16
+ *   B5-B10 the FFN seam and the MoE (moe_half)
+ * Rounding to bf16 happens exactly at the arrows; everything between is unrounded.
+ * Returns 0, or -1 on a bad cache view / unmapped page. */
+int orc_layer(const orc_spec *sp, const orc_weights *w, const orc_step *st, orc_trace *tr) {
+  int R = st->rows, H = sp->hidden, qr = sp->q_rank, kvd = sp->kv_dim, orank = sp->o_rank;
+  int QW = sp->n_q_heads * sp->head_dim, A = qr + kvd;
+  int rc = 0;
+  if (check_cache_view(sp, st)) return -1;
+
+  uint16_t *xn = malloc((size_t)R * H * 2), *qkv = malloc((size_t)R * A * 2);
+  uint16_t *qlat = malloc((size_t)R * qr * 2), *kv = malloc((size_t)R * kvd * 2);
+  uint16_t *qlatn = malloc((size_t)R * qr * 2), *kvn = malloc((size_t)R * kvd * 2);
+  uint16_t *q = malloc((size_t)R * QW * 2), *o = malloc((size_t)R * QW * 2);
+  uint16_t *oa = malloc((size_t)R * orank * 2), *h = malloc((size_t)R * H * 2);
+  int maxw = A;
+  if (QW > maxw) maxw = QW;
+  if (H > maxw) maxw = H;
+  if (orank > maxw) maxw = orank;
+  double *f = malloc((size_t)R * maxw * sizeof(double));
+
+  /* K1: attention front */
+  orc_rmsnorm(st->x, w->attn_norm, R, H, sp->eps, xn);                         /* A1 */
+  orc_gemv_mxfp8(xn, R, w->wqkv, w->wqkv_s, A, H, f);                          /* A2 */
+  round_rows(f, (size_t)R * A, qkv);
+  for (int r = 0; r < R; r++) {
+    memcpy(qlat + (size_t)r * qr, qkv + (size_t)r * A, (size_t)qr * 2);
+    memcpy(kv + (size_t)r * kvd, qkv + (size_t)r * A + qr, (size_t)kvd * 2);
+  }
+  orc_rmsnorm(qlat, w->q_norm, R, qr, sp->eps, qlatn);                         /* A3 */
+  orc_rmsnorm(kv, w->kv_norm, R, kvd, sp->eps, kvn);
+  if (orc_kv_insert(sp, st, kvn)) rc = -1;                                     /* A4 */
+  orc_gemv_mxfp8(qlatn, R, w->wq_b, w->wq_b_s, QW, qr, f);                     /* A5 */
+  round_rows(f, (size_t)R * QW, q);
+
+  /* K2: attention back, FFN seam, MoE */
+  if (orc_attention(sp, st, q, o)) rc = -1;                                    /* B1-B2 */
+  orc_gemv_mxfp8(o, R, w->wo_a, w->wo_a_s, orank, QW, f);                      /* B3 */
+  round_rows(f, (size_t)R * orank, oa);
+  orc_gemv_mxfp8(oa, R, w->wo_b, w->wo_b_s, H, orank, f);                      /* B4 */
+  for (size_t i = 0; i < (size_t)R * H; i++) h[i] = orc_bf16_bits(orc_bf16_value(st->x[i]) + f[i]);
+  uint16_t *out = tr && tr->out ? tr->out : malloc((size_t)R * H * 2);
+  moe_half(sp, w, st->x, st->positions, st->force_idx, R, h, out, tr);         /* B5-B10 */
 
   if (tr) {
 #define KEEP(dst, src, n) if (tr->dst) memcpy(tr->dst, src, n)
@@ -536,19 +561,31 @@ int orc_layer(const orc_spec *sp, const orc_weights *w, const orc_step *st, orc_
     KEEP(o, o, (size_t)R * QW * 2);
     KEEP(oa, oa, (size_t)R * orank * 2);
     KEEP(h, h, (size_t)R * H * 2);
-    KEEP(u, u, (size_t)R * H * 2);
-    KEEP(logits, logits, (size_t)R * E * sizeof(float));
-    KEEP(probs, probs, (size_t)R * E * sizeof(double));
-    KEEP(topk_idx, idx, (size_t)R * K * sizeof(int32_t));
-    KEEP(topk_w, wt, (size_t)R * K * sizeof(double));
-    KEEP(t_s, ts, (size_t)R * Is * 2);
-    KEEP(y_s, ys, (size_t)R * H * sizeof(double));
-    KEEP(y_r, yr, (size_t)R * H * sizeof(double));
 #undef KEEP
   }
   if (!(tr && tr->out)) free(out);
   free(xn), free(qkv), free(qlat), free(kv), free(qlatn), free(kvn), free(q), free(o), free(oa);
-  free(h), free(u), free(ts), free(f), free(ys), free(yr), free(logits);
-  free(probs), free(idx), free(wt), free(yslot), free(xe), free(te), free(yo), free(who);
+  free(h), free(f);
   return rc;
+}
+
+/* The FFN launch of one step (launch table, row FFN: for the layers whose attention runs
+ * elsewhere, "the attention TP all-reduce ... then K2's FFN seam and MoE").  `a` is the
+ * attention block's output for each row, bf16 [rows, H] (wo_b's output; on one GPU the
+ * all-reduce of the tensor-parallel partials is the identity, so `a` is already the sum).
+ * Reading: the residual is h = bf16(x + a), formed in unrounded arithmetic from the two
+ * bf16 inputs, as B4 forms it from x and wo_b's unrounded output; then B5-B10 exactly as in
+ * orc_layer.  Pad rows (positions < 0) output x.  No cache is touched; only the FFN fields
+ * of `w` (ffn_norm, router, sh_*, ex_*) are read, and the attention fields of `sp` are not. */
+void orc_ffn_layer(const orc_spec *sp, const orc_weights *w, const uint16_t *x, const uint16_t *a,
+                   const int32_t *positions, const int32_t *force_idx, int rows,
+                   orc_trace *tr) {
+  size_t n = (size_t)rows * sp->hidden;
+  uint16_t *h = malloc(n * 2);
+  for (size_t i = 0; i < n; i++) h[i] = orc_bf16_bits(orc_bf16_value(x[i]) + orc_bf16_value(a[i]));
+  uint16_t *out = tr && tr->out ? tr->out : malloc(n * 2);
+  moe_half(sp, w, x, positions, force_idx, rows, h, out, tr);
+  if (tr && tr->h) memcpy(tr->h, h, n * 2);
+  if (!(tr && tr->out)) free(out);
+  free(h);
 }

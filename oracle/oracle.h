@@ -100,6 +100,9 @@ void orc_ffn(const uint16_t *x, int rows, int fmt4, const uint8_t *gu, const uin
              const uint8_t *d, const uint8_t *d_s, int inter, int hidden, double clamp,
              uint16_t *t, double *y);
 int orc_layer(const orc_spec *sp, const orc_weights *w, const orc_step *st, orc_trace *tr);
+void orc_ffn_layer(const orc_spec *sp, const orc_weights *w, const uint16_t *x, const uint16_t *a,
+                   const int32_t *positions, const int32_t *force_idx, int rows,
+                   orc_trace *tr);
 
 void orc_set_threads(int n);
 int orc_get_threads(void);
