@@ -136,14 +136,49 @@ typedef struct {
 
 /* Validates spec and weights on the current CUDA device, allocates the scratch arena and
  * status word, and returns a handle.  Fails with MONO_ERR_UNSUPPORTED_DEVICE on a GPU
- * other than compute capability 10.3. */
+ * other than compute capability 10.3.
+ * The attention weights (attn_norm, q_norm, kv_norm, wqkv, wq_b, wo_a, wo_b and their
+ * scales) are all given or all NULL.  All NULL builds an FFN-only handle for the layers whose
+ * attention runs elsewhere: it accepts mono_ffn_step only, reads only the FFN fields of the
+ * spec (hidden, n_experts, topk, moe_inter, shared_inter, max_rows, eps, swiglu_clamp,
+ * routed_scale) and allocates no attention scratch.  Some but not all of them NULL is
+ * MONO_ERR_INVALID_ARG. */
 int mono_layer_build(const mono_layer_spec *spec, const mono_layer_weights *weights,
                      mono_layer_t **out);
 
 /* Enqueues one layer step on `stream` (a cudaStream_t; NULL = the legacy default stream).
  * Validates the arguments on the host and returns an error before enqueuing anything if
- * they are wrong.  Device-side faults (an unmapped page) set the status word instead. */
+ * they are wrong.  Device-side faults (an unmapped page) set the status word instead.
+ * MONO_ERR_INVALID_ARG on an FFN-only handle. */
 int mono_layer_step(mono_layer_t *h, const mono_step_args *args, void *stream);
+
+/*
+ * The FFN launch ("Mono decode layer for DeepSeek-V4.1-Flash on MI355X", section Purpose,
+ * launch table, row FFN; section Scope): for a layer whose attention runs elsewhere, the
+ * residual after attention and then K2's FFN seam and MoE -- the second half of
+ * mono_layer_step, with the same kernels.  Per row: h = bf16(x_in + attn_in), u =
+ * RMSNorm(h, ffn_norm), the f32 router and top-k, the MXFP8 shared expert and the MXFP4
+ * routed experts on u, x_out = bf16(h + shared + weighted routed sum); pad rows (positions
+ * < 0) are not routed and x_out = x_in.  The pages' attention all-reduce of wo_b's
+ * tensor-parallel partials is the identity on one GPU: attn_in is the whole attention output.
+ * Every pointer is a DEVICE pointer, 16-byte aligned; bf16 rows are [rows, H] row-major.
+ * Works on full and on FFN-only handles; validates on the host before enqueuing anything;
+ * allocates nothing and does no host synchronisation (graph-capturable), like a step.
+ * MONO_BUF_H then holds h and MONO_BUF_U .. MONO_BUF_YR this step's values; the attention
+ * buffers are untouched.  With profiling events set, it records events[7 + i] before its
+ * i-th launch (launch names 7..14 of the step list) and events[15] after the last.
+ */
+typedef struct {
+  const void *x_in;          /* bf16 [rows, H] residual stream entering the layer */
+  const void *attn_in;       /* bf16 [rows, H] attention output (wo_b's, all-reduced) */
+  void *x_out;               /* bf16 [rows, H]; may equal x_in or attn_in */
+  const int32_t *positions;  /* [rows] token position, < 0 for a pad row */
+  int32_t rows;              /* 1 <= rows <= max_rows */
+  int32_t *topk_idx_out;     /* optional [rows, topk] chosen experts (-1 on pad rows) */
+  float *topk_w_out;         /* optional [rows, topk] their weights */
+} mono_ffn_args;
+
+int mono_ffn_step(mono_layer_t *h, const mono_ffn_args *args, void *stream);
 
 /* Reads the device status word (synchronously; call after the step's stream has
  * finished).  Returns the MONO_STATUS_* bits (>= 0) or a negative error code; clears the

@@ -28,6 +28,8 @@ SPEC_INT_FIELDS = ["hidden", "n_q_heads", "head_dim", "kv_dim", "q_rank", "o_ran
                    "topk", "moe_inter", "shared_inter", "window", "swa_width", "causal",
                    "block_size", "kv_record_bytes", "max_rows"]
 SPEC_FLOAT_FIELDS = ["eps", "swiglu_clamp", "routed_scale"]
+ATTN_WEIGHT_FIELDS = ["attn_norm", "q_norm", "kv_norm", "wqkv", "wqkv_s", "wq_b", "wq_b_s", "wo_a",
+                      "wo_a_s", "wo_b", "wo_b_s"]
 WEIGHT_FIELDS = ["attn_norm", "q_norm", "kv_norm", "ffn_norm", "wqkv", "wqkv_s", "wq_b", "wq_b_s",
                  "wo_a", "wo_a_s", "wo_b", "wo_b_s", "router", "sh_gu", "sh_gu_s", "sh_d", "sh_d_s",
                  "ex_gu", "ex_gu_s", "ex_d", "ex_d_s"]
@@ -50,7 +52,14 @@ class StepArgs(C.Structure):
                 ("topk_w_out", C.c_void_p)]
 
 
-EXPORTS = ["mono_layer_build", "mono_layer_step", "mono_layer_status", "mono_layer_free",
+class FfnArgs(C.Structure):
+    _fields_ = [("x_in", C.c_void_p), ("attn_in", C.c_void_p), ("x_out", C.c_void_p),
+                ("positions", C.c_void_p), ("rows", C.c_int32), ("topk_idx_out", C.c_void_p),
+                ("topk_w_out", C.c_void_p)]
+
+
+EXPORTS = ["mono_layer_build", "mono_layer_step", "mono_ffn_step", "mono_layer_status",
+           "mono_layer_free",
            "mono_layer_strerror", "mono_layer_buffer", "mono_layer_read_buffer",
            "mono_layer_launches_per_step", "mono_layer_launch_name",
            "mono_layer_set_profile_events", "mono_attention_noalloc"]
@@ -74,6 +83,7 @@ def lib() -> C.CDLL:
         L = C.CDLL(LIB_PATH)
         L.mono_layer_build.argtypes = [C.POINTER(Spec), C.POINTER(Weights), C.POINTER(C.c_void_p)]
         L.mono_layer_step.argtypes = [C.c_void_p, C.POINTER(StepArgs), C.c_void_p]
+        L.mono_ffn_step.argtypes = [C.c_void_p, C.POINTER(FfnArgs), C.c_void_p]
         L.mono_layer_status.argtypes = [C.c_void_p, C.c_int]
         L.mono_layer_free.argtypes = [C.c_void_p]
         L.mono_layer_free.restype = None
@@ -109,11 +119,12 @@ def make_spec(spec: dict, max_rows: int | None = None) -> Spec:
 
 class Layer:
     """A built layer: owns the C handle.  ``weights`` maps field names to CUDA tensors that
-    must outlive the Layer (they are read in place)."""
+    must outlive the Layer (they are read in place).  Without any of the attention weights
+    the handle is FFN-only and runs ``ffn_step`` alone."""
 
     def __init__(self, spec: dict, weights: dict, max_rows: int | None = None):
         self.spec = dict(spec)
-        self._weights = {k: weights[k] for k in WEIGHT_FIELDS}  # keep alive
+        self._weights = {k: weights.get(k) for k in WEIGHT_FIELDS}  # keep alive
         self._h = C.c_void_p()
         w = Weights(**{k: _ptr(v) for k, v in self._weights.items()})
         rc = lib().mono_layer_build(C.byref(make_spec(spec, max_rows)), C.byref(w), C.byref(self._h))
@@ -147,6 +158,23 @@ class Layer:
         rc = lib().mono_layer_step(self._h, C.byref(args), C.c_void_p(stream_handle))
         if rc != MONO_OK:
             raise MonoError(rc, "mono_layer_step")
+
+    def ffn_step(self, x_in, attn_in, x_out, positions, stream=None, topk_idx_out=None,
+                 topk_w_out=None) -> None:
+        """Enqueues one FFN launch (residual x_in + attn_in, then the FFN seam and the MoE)
+        on `stream` (default: torch's current stream)."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        a = FfnArgs(x_in=_ptr(x_in), attn_in=_ptr(attn_in), x_out=_ptr(x_out),
+                    positions=_ptr(positions), rows=x_in.shape[0], topk_idx_out=_ptr(topk_idx_out),
+                    topk_w_out=_ptr(topk_w_out))
+        self.ffn_step_raw(a, stream.cuda_stream)
+
+    def ffn_step_raw(self, args: FfnArgs, stream_handle: int) -> None:
+        rc = lib().mono_ffn_step(self._h, C.byref(args), C.c_void_p(stream_handle))
+        if rc != MONO_OK:
+            raise MonoError(rc, "mono_ffn_step")
 
     def status(self, clear: bool = False) -> int:
         rc = lib().mono_layer_status(self._h, int(clear))
@@ -204,4 +232,4 @@ class Layer:
 
 
 __all__ = ["Layer", "MonoError", "lib", "strerror", "make_spec", "Spec", "Weights", "StepArgs",
-           "BUF", "EXPORTS", "LIB_PATH"]
+           "FfnArgs", "BUF", "EXPORTS", "LIB_PATH", "ATTN_WEIGHT_FIELDS"]

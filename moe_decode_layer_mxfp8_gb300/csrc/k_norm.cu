@@ -33,6 +33,27 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(NormArgs a) {
     const int i = (c * NORM_THREADS + tid) * 8;
     if (i < a.dim) xv[c] = *reinterpret_cast<const uint4*>(x + i);
   }
+  if (a.resid) {
+    // residual first: h = bf16(x + resid).  The f32 sum of two bf16 values rounds to the
+    // same bf16 as their exact sum (an f32 rounding error only arises when the exponents
+    // differ by more than 16, far from any bf16 rounding midpoint).
+    const __nv_bfloat16* rr = a.resid + (size_t)r * a.resid_ld;
+    __nv_bfloat16* hs = a.sum_out + (size_t)r * a.sum_ld;
+#pragma unroll
+    for (int c = 0; c < NORM_CHUNKS; ++c) {
+      const int i = (c * NORM_THREADS + tid) * 8;
+      if (i < a.dim) {
+        float f[8], g[8];
+        bf16x8_to_f32(xv[c], f);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(rr + i), g);
+        xv[c].x = pack_bf16x2(f[0] + g[0], f[1] + g[1]);
+        xv[c].y = pack_bf16x2(f[2] + g[2], f[3] + g[3]);
+        xv[c].z = pack_bf16x2(f[4] + g[4], f[5] + g[5]);
+        xv[c].w = pack_bf16x2(f[6] + g[6], f[7] + g[7]);
+        *reinterpret_cast<uint4*>(hs + i) = xv[c];
+      }
+    }
+  }
   float ss = 0.0f;
 #pragma unroll
   for (int c = 0; c < NORM_CHUNKS; ++c) {

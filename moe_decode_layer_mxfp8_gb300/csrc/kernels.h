@@ -40,6 +40,12 @@ struct NormArgs {
   float eps;
   __half* out;
   int out_ld;
+  // optional residual: when resid is set, the kernel normalises h = bf16(in + resid) and
+  // also stores h to sum_out
+  const __nv_bfloat16* resid = nullptr;
+  int resid_ld = 0;
+  __nv_bfloat16* sum_out = nullptr;
+  int sum_ld = 0;
 };
 
 struct QkvNormInsertArgs {

@@ -23,6 +23,7 @@ using namespace mono;
 namespace {
 
 constexpr int kLaunchesPerStep = 15;
+constexpr int kFfnFirstLaunch = 7;  // the FFN launch runs launches 7..14 of the list
 const char* const kLaunchNames[kLaunchesPerStep] = {
     "attn_norm", "wqkv", "qkv_norm_insert", "wq_b", "attention", "wo_a", "wo_b", "ffn_norm",
     "router", "topk_group", "shared_gate_up", "shared_down", "expert_gate_up", "expert_down",
@@ -42,6 +43,7 @@ struct DensePlan {
 struct mono_layer {
   mono_layer_spec spec;
   mono_layer_weights w;
+  bool ffn_only = false;  // built without attention weights: FFN launches only
   int device = 0, num_sms = 0;
   uint8_t* arena = nullptr;
   size_t arena_bytes = 0;
@@ -101,27 +103,31 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long row_by
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-int check_spec(const mono_layer_spec& s) {
-  const int qw = s.n_q_heads * s.head_dim;
-  if (s.hidden <= 0 || s.n_q_heads <= 0 || s.q_rank <= 0 || s.o_rank <= 0 || s.kv_dim <= 0 ||
-      s.moe_inter <= 0 || s.shared_inter <= 0 || s.n_experts <= 0 || s.block_size <= 0)
+// FFN fields: hidden, the experts, the intermediates, max_rows.  Attention fields only when
+// the handle holds attention weights.
+int check_spec(const mono_layer_spec& s, bool ffn_only) {
+  if (s.hidden <= 0 || s.moe_inter <= 0 || s.shared_inter <= 0 || s.n_experts <= 0)
     return MONO_ERR_UNSUPPORTED_DIMS;
   // reduction lengths are whole 128-element stages
-  if (s.hidden % 128 || s.q_rank % 128 || s.o_rank % 128 || qw % 128 || s.moe_inter % 128 ||
-      s.shared_inter % 128)
+  if (s.hidden % 128 || s.moe_inter % 128 || s.shared_inter % 128) return MONO_ERR_UNSUPPORTED_DIMS;
+  if (s.hidden > 8192) return MONO_ERR_UNSUPPORTED_DIMS;  // row kernels
+  if (s.topk < 1 || s.topk > 8 || s.topk > s.n_experts || s.n_experts > MAX_EXPERTS)
     return MONO_ERR_UNSUPPORTED_DIMS;
+  if (s.max_rows < 1 || s.max_rows > 48) return MONO_ERR_TOO_MANY_ROWS;
+  if (ffn_only) return MONO_OK;
+  const int qw = s.n_q_heads * s.head_dim;
+  if (s.n_q_heads <= 0 || s.q_rank <= 0 || s.o_rank <= 0 || s.kv_dim <= 0 || s.block_size <= 0)
+    return MONO_ERR_UNSUPPORTED_DIMS;
+  if (s.q_rank % 128 || s.o_rank % 128 || qw % 128) return MONO_ERR_UNSUPPORTED_DIMS;
   if (s.kv_dim % 32 || s.kv_dim > 1024) return MONO_ERR_UNSUPPORTED_DIMS;
-  if (s.hidden > 8192 || s.q_rank > 4096) return MONO_ERR_UNSUPPORTED_DIMS;  // row kernels
+  if (s.q_rank > 4096) return MONO_ERR_UNSUPPORTED_DIMS;  // row kernels
   if (s.head_dim != 64 && s.head_dim != 128) return MONO_ERR_UNSUPPORTED_DIMS;
   if (s.kv_dim % s.head_dim) return MONO_ERR_UNSUPPORTED_DIMS;
   const int G = s.kv_dim / s.head_dim;
   if (s.n_q_heads % G || s.n_q_heads / G > 16) return MONO_ERR_UNSUPPORTED_DIMS;
-  if (s.topk < 1 || s.topk > 8 || s.topk > s.n_experts || s.n_experts > MAX_EXPERTS)
-    return MONO_ERR_UNSUPPORTED_DIMS;
   if (s.window < 1 || s.window > 1024 || s.swa_width < 1 || s.swa_width > 1024)
     return MONO_ERR_UNSUPPORTED_DIMS;
   if (s.kv_record_bytes < s.kv_dim + 4 || s.kv_record_bytes % 16) return MONO_ERR_UNSUPPORTED_DIMS;
-  if (s.max_rows < 1 || s.max_rows > 48) return MONO_ERR_TOO_MANY_ROWS;
   return MONO_OK;
 }
 
@@ -158,13 +164,21 @@ const char* mono_layer_strerror(int code) {
 int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, mono_layer_t** out) {
   if (!spec || !wt || !out) return MONO_ERR_INVALID_ARG;
   *out = nullptr;
-  int rc = check_spec(*spec);
+  const void* attn_ptrs[] = {wt->attn_norm, wt->q_norm, wt->kv_norm, wt->wqkv, wt->wqkv_s,
+                             wt->wq_b,      wt->wq_b_s, wt->wo_a,    wt->wo_a_s, wt->wo_b,
+                             wt->wo_b_s};
+  const void* ffn_ptrs[] = {wt->ffn_norm, wt->router, wt->sh_gu, wt->sh_gu_s, wt->sh_d,
+                            wt->sh_d_s,   wt->ex_gu,  wt->ex_gu_s, wt->ex_d,  wt->ex_d_s};
+  int n_attn = 0;
+  for (const void* p : attn_ptrs) n_attn += p != nullptr;
+  if (n_attn != 0 && n_attn != (int)(sizeof(attn_ptrs) / sizeof(attn_ptrs[0])))
+    return MONO_ERR_INVALID_ARG;  // attention weights: all or none
+  const bool ffn_only = n_attn == 0;
+  int rc = check_spec(*spec, ffn_only);
   if (rc) return rc;
-  const void* ptrs[] = {wt->attn_norm, wt->q_norm, wt->kv_norm, wt->ffn_norm, wt->wqkv, wt->wqkv_s,
-                        wt->wq_b,      wt->wq_b_s,   wt->wo_a,   wt->wo_a_s,    wt->wo_b, wt->wo_b_s,
-                        wt->router,    wt->sh_gu,    wt->sh_gu_s, wt->sh_d,     wt->sh_d_s, wt->ex_gu,
-                        wt->ex_gu_s,   wt->ex_d,     wt->ex_d_s};
-  for (const void* p : ptrs) {
+  for (const void* p : attn_ptrs)
+    if (p && !aligned16(p)) return MONO_ERR_BAD_ALIGNMENT;
+  for (const void* p : ffn_ptrs) {
     if (!p) return MONO_ERR_INVALID_ARG;
     if (!aligned16(p)) return MONO_ERR_BAD_ALIGNMENT;
   }
@@ -181,12 +195,18 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
   if (!h) return MONO_ERR_OUT_OF_MEMORY;
   h->spec = *spec;
   h->w = *wt;
+  h->ffn_only = ffn_only;
   h->device = dev;
   h->num_sms = prop.multiProcessorCount;
   const mono_layer_spec& s = h->spec;
   const int R = s.max_rows, H = s.hidden, E = s.n_experts, K = s.topk;
-  const int QW = s.n_q_heads * s.head_dim, A = s.q_rank + s.kv_dim;
-  const int G = s.kv_dim / s.head_dim;
+  // an FFN-only handle leaves the attention fields unread and sizes no attention buffers
+  const int QW = ffn_only ? 0 : s.n_q_heads * s.head_dim;
+  const int A = ffn_only ? 0 : s.q_rank + s.kv_dim;
+  const int G = ffn_only ? 0 : s.kv_dim / s.head_dim;
+  const int q_rank = ffn_only ? 0 : s.q_rank, kv_dim = ffn_only ? 0 : s.kv_dim;
+  const int o_rank = ffn_only ? 0 : s.o_rank, n_q = ffn_only ? 0 : s.n_q_heads;
+  const int head_dim = ffn_only ? 0 : s.head_dim;
 
   // dense GEMV plans: K split until the tiles cover the SMs
   struct Def {
@@ -198,7 +218,7 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
                      {wt->wo_b, wt->wo_b_s, H, s.o_rank, 0},
                      {wt->sh_gu, wt->sh_gu_s, 2 * s.shared_inter, H, s.shared_inter},
                      {wt->sh_d, wt->sh_d_s, H, s.shared_inter, 0}};
-  for (int i = 0; i < D_COUNT; ++i) {
+  for (int i = ffn_only ? D_SHGU : 0; i < D_COUNT; ++i) {
     DensePlan& d = h->dense[i];
     d.scales = defs[i].sc;
     d.N = defs[i].N;
@@ -221,8 +241,8 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
     return MONO_ERR_CUDA;
   }
   const int width = std::max(s.causal ? s.window : s.swa_width, s.window);
-  h->attn_min_splits = (width + 127) / 128;
-  const int attn_splits_max = ATTN_MAX_SPLITS;
+  h->attn_min_splits = ffn_only ? 0 : (width + 127) / 128;
+  const int attn_splits_max = ffn_only ? 0 : ATTN_MAX_SPLITS;
 
   // scratch arena
   size_t off = 0;
@@ -232,8 +252,9 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
     return o;
   };
   const size_t sizes[MONO_BUF_COUNT] = {
-      (size_t)R * H * 2,  (size_t)R * A * 2,      (size_t)R * s.q_rank * 2, (size_t)R * s.kv_dim * 2,
-      (size_t)R * QW * 2, (size_t)R * QW * 2,     (size_t)R * s.o_rank * 2, (size_t)R * H * 2,
+      (size_t)R * (ffn_only ? 0 : H) * 2, (size_t)R * A * 2, (size_t)R * q_rank * 2,
+      (size_t)R * kv_dim * 2, (size_t)R * QW * 2, (size_t)R * QW * 2, (size_t)R * o_rank * 2,
+      (size_t)R * H * 2,
       (size_t)R * H * 2,  (size_t)R * E * 4,      (size_t)R * K * 4,        (size_t)R * K * 4,
       (size_t)R * K * 4,  (size_t)R * s.shared_inter * 2, (size_t)R * H * 4,
       (size_t)R * K * s.moe_inter * 2, (size_t)R * K * H * 4};
@@ -242,7 +263,7 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
     h->buf_off[b] = take(sizes[b]);
   }
   const size_t o_ctr = take((size_t)R * G * 4);
-  const size_t o_part = take((size_t)R * s.n_q_heads * attn_splits_max * (s.head_dim + ATTN_PART_HEAD) * 4);
+  const size_t o_part = take((size_t)R * n_q * attn_splits_max * (head_dim + ATTN_PART_HEAD) * 4);
   const size_t o_status = take(16);
   const size_t o_route = take(sizeof(RouteInfo));
   const size_t o_perm = take((size_t)R * K * 4);
@@ -286,7 +307,7 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
   // once even while the previous kernels' last CTAs drain (items are assigned statically)
   h->ex_clusters = gemm_max_clusters({4, 1, 2}, EXPERT_CLUSTER) * 7 / 8;
   if (h->ex_clusters < 1) rc = MONO_ERR_CUDA;
-  if (attention_prepare(s.head_dim) != cudaSuccess) rc = MONO_ERR_CUDA;
+  if (!ffn_only && attention_prepare(s.head_dim) != cudaSuccess) rc = MONO_ERR_CUDA;
   if (router_prepare() != cudaSuccess) rc = MONO_ERR_CUDA;
   if (!rc && (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
               cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
@@ -357,8 +378,217 @@ int mono_layer_set_profile_events(mono_layer_t* h, void* const* events, int n_ev
   return MONO_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Enqueues the launches of a step in order, recording the profiling event of each launch
+// index before it when profiling is on.
+struct Enqueue {
+  mono_layer* h;
+  cudaStream_t stream;
+  int next;  // launch index (into the layer's launch-name list) of the next launch
+  template <class F>
+  int operator()(F&& launch) {
+    if (h->profiling) {
+      const cudaError_t e = cudaEventRecord(h->prof[next], stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    ++next;
+    const cudaError_t e = launch();
+    return e == cudaSuccess ? MONO_OK : cuda_fail(e);
+  }
+};
+
+#define TRY(x)                          \
+  do {                                  \
+    const int rc_ = (x);                \
+    if (rc_ != MONO_OK) return rc_;     \
+  } while (0)
+#define TRY_CUDA(x)                                 \
+  do {                                              \
+    const cudaError_t e_ = (x);                     \
+    if (e_ != cudaSuccess) return cuda_fail(e_);    \
+  } while (0)
+
+// One MXFP8 dense GEMV of the layer over R rows.
+cudaError_t dense_launch(const mono_layer* h, int id, int R, const __half* act, int act_ld,
+                         int epi, void* outp, int out_ld, const __nv_bfloat16* resid,
+                         const Launch& L) {
+  const DensePlan& d = h->dense[id];
+  const int nt = nt_bucket(R);
+  GemmParams p = {};
+  p.scales = d.scales;
+  p.scale_ld = d.K / 32;
+  p.K = d.K;
+  p.N = d.N;
+  p.swiglu_I = d.swiglu_I;
+  p.act = act;
+  p.act_ld = act_ld;
+  p.dense_rows = R;
+  p.n_tiles = d.n_tiles;
+  p.ksplit = d.ksplit;
+  p.epi = epi;
+  p.out = outp;
+  p.out_ld = out_ld;
+  p.resid = resid;
+  p.resid_ld = h->spec.hidden;
+  p.clamp = h->spec.swiglu_clamp;
+  p.status = h->status;
+  const int clusters = std::min(d.n_tiles, d.max_clusters[nt]);
+  return launch_gemm(L, {8, nt}, d.map, p, clusters * d.ksplit, d.ksplit);
+}
+
+// One MXFP4 routed-expert GEMM over the R * topk (row, slot) pairs grouped by expert.
+cudaError_t expert_launch(const mono_layer* h, int R, const CUtensorMap& map, const uint8_t* sc,
+                          int Kdim, int rows_per_mat, int swiglu, int n_tiles, const __half* act,
+                          int act_ld, const int* rowmap, int epi, void* outp, int out_ld,
+                          const Launch& L) {
+  const int K = h->spec.topk;
+  GemmParams p = {};
+  p.scales = sc;
+  p.scale_ld = Kdim / 32;
+  p.K = Kdim;
+  p.N = rows_per_mat;
+  p.rows_per_mat = rows_per_mat;
+  p.swiglu_I = swiglu;
+  p.act = act;
+  p.act_ld = act_ld;
+  p.act_rowmap = rowmap;
+  p.n_tiles = n_tiles;
+  // small steps: clusters that split the K of each item when the items are few
+  const bool small = R * K <= EXPERT_SMALL_SLOTS;
+  p.ksplit = small ? EXPERT_CLUSTER : 1;
+  p.n_slots = R * K;
+  p.route = h->route;
+  p.epi = epi;
+  p.out = outp;
+  p.out_ld = out_ld;
+  p.clamp = h->spec.swiglu_clamp;
+  p.status = h->status;
+  if (small)
+    return launch_gemm(L, {4, 1, 2}, map, p, h->ex_clusters * EXPERT_CLUSTER, EXPERT_CLUSTER);
+  return launch_gemm(L, {4, 1, 1}, map, p, h->ex_ctas, 1);
+}
+
+// Inputs of the FFN half of a step (shared by the whole-layer step and the FFN launch).
+struct MoeIn {
+  NormArgs seam;              // the FFN-seam norm; it writes u (and h, when it forms the residual)
+  const __nv_bfloat16* x;     // the layer input, returned unchanged on pad rows
+  const int32_t* positions;
+  int R;
+  int32_t* topk_idx_out;
+  float* topk_w_out;
+  void* x_out;
+};
+
+// K2's FFN half: FFN-seam norm -> router -> top-k + grouping, the shared expert on the side
+// stream, routed gate_up / down -> final combine.  Launch indices 7..14 of the layer's list.
+int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
+  const mono_layer_spec& s = h->spec;
+  const cudaStream_t stream = run.stream;
+  const Launch L{stream, !h->profiling};
+  const int R = m.R, H = s.hidden, E = s.n_experts, K = s.topk;
+  TRY(run([&] { return launch_rmsnorm(L, m.seam, R); }));
+  TRY(run([&] {
+    return launch_router(L, {h->buf<__half>(MONO_BUF_U), h->w.router, R, E, H, h->router_part});
+  }));
+  // The shared expert depends only on u: fork it onto the side stream after the router (whose
+  // CTAs are then resident before the shared expert's GEMM CTAs claim the SMs) so that it
+  // overlaps the top-k (and, in large steps, the routed experts).  While profiling,
+  // everything stays on one stream in launch-name order.
+  const bool fork = !h->profiling;
+  const Launch Ls{fork ? h->side : stream, !h->profiling};
+  if (fork) {
+    TRY_CUDA(cudaEventRecord(h->ev_fork, stream));
+    TRY_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
+  }
+  auto shared_expert = [&]() -> int {
+    TRY(run([&] {
+      return dense_launch(h, D_SHGU, R, h->buf<__half>(MONO_BUF_U), H, EPI_SWIGLU_F16,
+                          h->buf<void>(MONO_BUF_TS), s.shared_inter, nullptr, Ls);
+    }));
+    TRY(run([&] {
+      return dense_launch(h, D_SHD, R, h->buf<__half>(MONO_BUF_TS), s.shared_inter, EPI_F32,
+                          h->buf<void>(MONO_BUF_YS), H, nullptr, Ls);
+    }));
+    return MONO_OK;
+  };
+  // launch indices stay in name order although the shared expert is enqueued first
+  const int topk_no = run.next;
+  if (fork) {
+    run.next = topk_no + 1;
+    TRY(shared_expert());
+    TRY_CUDA(cudaEventRecord(h->ev_join, h->side));
+    run.next = topk_no;
+  }
+  {
+    TopkArgs t = {};
+    t.partial = h->router_part;
+    t.kslices = h->router_kslices;
+    t.logits = h->buf<float>(MONO_BUF_LOGITS);
+    t.positions = m.positions;
+    t.rows = R;
+    t.E = E;
+    t.k = K;
+    t.routed_scale = s.routed_scale;
+    t.topk_idx = h->buf<int>(MONO_BUF_TOPK_IDX);
+    t.topk_w = h->buf<float>(MONO_BUF_TOPK_W);
+    t.slot_pos = h->buf<int>(MONO_BUF_SLOT_POS);
+    t.perm = h->perm;
+    t.route = h->route;
+    t.user_idx = m.topk_idx_out;
+    t.user_w = m.topk_w_out;
+    t.status = h->status;
+    TRY(run([&] { return launch_topk(L, t); }));
+  }
+  // Large steps: the persistent expert GEMM starts right after the top-k and the shared
+  // expert joins before the final combine.  Small steps: the routed experts' clusters want
+  // every SM at once (items are assigned statically), so they wait for the shared expert.
+  const bool late_join = fork && R * K > EXPERT_SMALL_SLOTS;
+  if (fork) {
+    run.next += 2;
+    if (!late_join) TRY_CUDA(cudaStreamWaitEvent(stream, h->ev_join, 0));
+  } else {
+    TRY(shared_expert());
+  }
+  TRY(run([&] {
+    return expert_launch(h, R, h->map_ex_gu, h->w.ex_gu_s, H, 2 * s.moe_inter, s.moe_inter,
+                         s.moe_inter / BOX_ROWS, h->buf<__half>(MONO_BUF_U), H, h->perm,
+                         EPI_SWIGLU_F16, h->buf<void>(MONO_BUF_TR), s.moe_inter, L);
+  }));
+  TRY(run([&] {
+    return expert_launch(h, R, h->map_ex_d, h->w.ex_d_s, s.moe_inter, H, 0, H / TILE_M,
+                         h->buf<__half>(MONO_BUF_TR), s.moe_inter, nullptr, EPI_F32,
+                         h->buf<void>(MONO_BUF_YR), H, L);
+  }));
+  if (late_join) TRY_CUDA(cudaStreamWaitEvent(stream, h->ev_join, 0));
+  {
+    FinalArgs f = {};
+    f.x = m.x;
+    f.h = h->buf<__nv_bfloat16>(MONO_BUF_H);
+    f.ys = h->buf<float>(MONO_BUF_YS);
+    f.yr = h->buf<float>(MONO_BUF_YR);
+    f.slot_pos = h->buf<int>(MONO_BUF_SLOT_POS);
+    f.topk_w = h->buf<float>(MONO_BUF_TOPK_W);
+    f.positions = m.positions;
+    f.rows = R;
+    f.H = H;
+    f.k = K;
+    f.out = reinterpret_cast<__nv_bfloat16*>(m.x_out);
+    TRY(run([&] { return launch_final(L, f); }));
+  }
+  if (h->profiling) TRY_CUDA(cudaEventRecord(h->prof[kLaunchesPerStep], stream));
+  return MONO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) {
   if (!h || !a) return MONO_ERR_INVALID_ARG;
+  if (h->ffn_only) return MONO_ERR_INVALID_ARG;
   const mono_layer_spec& s = h->spec;
   const int R = a->rows;
   if (R < 1) return MONO_ERR_INVALID_ARG;
@@ -375,86 +605,20 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
 
   const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
   const Launch L{stream, !h->profiling};
-  int launch_no = 0;
-  const int H = s.hidden, E = s.n_experts, K = s.topk, QW = s.n_q_heads * s.head_dim;
+  Enqueue run{h, stream, 0};
+  const int H = s.hidden, QW = s.n_q_heads * s.head_dim;
   const int A = s.q_rank + s.kv_dim, G = s.kv_dim / s.head_dim;
-  const int nt = nt_bucket(R);
   const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(a->x_in);
-  cudaError_t e = cudaSuccess;
-#define RUN(call)                                                          \
-  do {                                                                     \
-    if (h->profiling) {                                                    \
-      e = cudaEventRecord(h->prof[launch_no], stream);                     \
-      if (e != cudaSuccess) return cuda_fail(e);                           \
-    }                                                                      \
-    ++launch_no;                                                           \
-    e = (call);                                                            \
-    if (e != cudaSuccess) return cuda_fail(e);                             \
-  } while (0)
-#define RUN_PLAIN(call)                        \
-  do {                                         \
-    e = (call);                                \
-    if (e != cudaSuccess) return cuda_fail(e); \
-  } while (0)
-
-  auto dense = [&](int id, const __half* act, int act_ld, int epi, void* outp, int out_ld,
-                   const __nv_bfloat16* resid, const Launch& LL) {
-    const DensePlan& d = h->dense[id];
-    GemmParams p = {};
-    p.scales = d.scales;
-    p.scale_ld = d.K / 32;
-    p.K = d.K;
-    p.N = d.N;
-    p.swiglu_I = d.swiglu_I;
-    p.act = act;
-    p.act_ld = act_ld;
-    p.dense_rows = R;
-    p.n_tiles = d.n_tiles;
-    p.ksplit = d.ksplit;
-    p.epi = epi;
-    p.out = outp;
-    p.out_ld = out_ld;
-    p.resid = resid;
-    p.resid_ld = H;
-    p.clamp = s.swiglu_clamp;
-    p.status = h->status;
-    const int clusters = std::min(d.n_tiles, d.max_clusters[nt]);
-    return launch_gemm(LL, {8, nt}, d.map, p, clusters * d.ksplit, d.ksplit);
-  };
-  auto expert = [&](const CUtensorMap& map, const uint8_t* sc, int Kdim, int rows_per_mat,
-                    int swiglu, int n_tiles, const __half* act, int act_ld, const int* rowmap,
-                    int epi, void* outp, int out_ld) {
-    GemmParams p = {};
-    p.scales = sc;
-    p.scale_ld = Kdim / 32;
-    p.K = Kdim;
-    p.N = rows_per_mat;
-    p.rows_per_mat = rows_per_mat;
-    p.swiglu_I = swiglu;
-    p.act = act;
-    p.act_ld = act_ld;
-    p.act_rowmap = rowmap;
-    p.n_tiles = n_tiles;
-    // small steps: clusters that split the K of each item when the items are few
-    const bool small = R * K <= EXPERT_SMALL_SLOTS;
-    p.ksplit = small ? EXPERT_CLUSTER : 1;
-    p.n_slots = R * K;
-    p.route = h->route;
-    p.epi = epi;
-    p.out = outp;
-    p.out_ld = out_ld;
-    p.clamp = s.swiglu_clamp;
-    p.status = h->status;
-    if (small)
-      return launch_gemm(L, {4, 1, 2}, map, p, h->ex_clusters * EXPERT_CLUSTER, EXPERT_CLUSTER);
-    return launch_gemm(L, {4, 1, 1}, map, p, h->ex_ctas, 1);
-  };
 
   // ---------------------------------------------------------------- K1: attention front
-  RUN(launch_rmsnorm(L, {x, H, (const __nv_bfloat16*)h->w.attn_norm, H, s.eps,
-                         h->buf<__half>(MONO_BUF_XN), H}, R));
-  RUN(dense(D_WQKV, h->buf<__half>(MONO_BUF_XN), H, EPI_BF16, h->buf<void>(MONO_BUF_QKV), A,
-            nullptr, L));
+  TRY(run([&] {
+    return launch_rmsnorm(L, {x, H, (const __nv_bfloat16*)h->w.attn_norm, H, s.eps,
+                              h->buf<__half>(MONO_BUF_XN), H}, R);
+  }));
+  TRY(run([&] {
+    return dense_launch(h, D_WQKV, R, h->buf<__half>(MONO_BUF_XN), H, EPI_BF16,
+                        h->buf<void>(MONO_BUF_QKV), A, nullptr, L);
+  }));
   {
     QkvNormInsertArgs q = {};
     q.qkv = h->buf<__nv_bfloat16>(MONO_BUF_QKV);
@@ -476,10 +640,12 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     q.stride_tok = a->kv_stride_tok;
     q.num_blocks = a->kv_num_blocks;
     q.status = h->status;
-    RUN(launch_qkv_norm_insert(L, q, R));
+    TRY(run([&] { return launch_qkv_norm_insert(L, q, R); }));
   }
-  RUN(dense(D_WQB, h->buf<__half>(MONO_BUF_QLATN), s.q_rank, EPI_BF16, h->buf<void>(MONO_BUF_Q),
-            QW, nullptr, L));
+  TRY(run([&] {
+    return dense_launch(h, D_WQB, R, h->buf<__half>(MONO_BUF_QLATN), s.q_rank, EPI_BF16,
+                        h->buf<void>(MONO_BUF_Q), QW, nullptr, L);
+  }));
 
   // ---------------------------------------------------------------- K2: attention back
   {
@@ -508,97 +674,57 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     t.part = h->attn_part;
     t.counters = h->attn_counters;
     t.status = h->status;
-    RUN(launch_attention(L, t, s.head_dim, G));
+    TRY(run([&] { return launch_attention(L, t, s.head_dim, G); }));
   }
-  RUN(dense(D_WOA, h->buf<__half>(MONO_BUF_O), QW, EPI_F16, h->buf<void>(MONO_BUF_OA), s.o_rank,
-            nullptr, L));
-  RUN(dense(D_WOB, h->buf<__half>(MONO_BUF_OA), s.o_rank, EPI_RESID_BF16, h->buf<void>(MONO_BUF_H),
-            H, x, L));
+  TRY(run([&] {
+    return dense_launch(h, D_WOA, R, h->buf<__half>(MONO_BUF_O), QW, EPI_F16,
+                        h->buf<void>(MONO_BUF_OA), s.o_rank, nullptr, L);
+  }));
+  TRY(run([&] {
+    return dense_launch(h, D_WOB, R, h->buf<__half>(MONO_BUF_OA), s.o_rank, EPI_RESID_BF16,
+                        h->buf<void>(MONO_BUF_H), H, x, L);
+  }));
 
   // ---------------------------------------------------------------- K2: FFN seam and MoE
-  RUN(launch_rmsnorm(L, {h->buf<__nv_bfloat16>(MONO_BUF_H), H, (const __nv_bfloat16*)h->w.ffn_norm,
-                         H, s.eps, h->buf<__half>(MONO_BUF_U), H}, R));
-  RUN(launch_router(L, {h->buf<__half>(MONO_BUF_U), h->w.router, R, E, H, h->router_part}));
-  // The shared expert depends only on u: fork it onto the side stream after the router (whose
-  // CTAs are then resident before the shared expert's GEMM CTAs claim the SMs) so that it
-  // overlaps the top-k (and, in large steps, the routed experts).  While profiling,
-  // everything stays on one stream in launch-name order.
-  const bool fork = !h->profiling;
-  const Launch Ls{fork ? h->side : stream, !h->profiling};
-  if (fork) {
-    RUN_PLAIN(cudaEventRecord(h->ev_fork, stream));
-    RUN_PLAIN(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
-  }
-  auto shared_expert = [&]() -> int {
-    RUN(dense(D_SHGU, h->buf<__half>(MONO_BUF_U), H, EPI_SWIGLU_F16, h->buf<void>(MONO_BUF_TS),
-              s.shared_inter, nullptr, Ls));
-    RUN(dense(D_SHD, h->buf<__half>(MONO_BUF_TS), s.shared_inter, EPI_F32,
-              h->buf<void>(MONO_BUF_YS), H, nullptr, Ls));
-    return MONO_OK;
-  };
-  if (fork) {
-    const int rs = shared_expert();
-    if (rs != MONO_OK) return rs;
-    RUN_PLAIN(cudaEventRecord(h->ev_join, h->side));
-  }
-  {
-    TopkArgs t = {};
-    t.partial = h->router_part;
-    t.kslices = h->router_kslices;
-    t.logits = h->buf<float>(MONO_BUF_LOGITS);
-    t.positions = a->positions;
-    t.rows = R;
-    t.E = E;
-    t.k = K;
-    t.routed_scale = s.routed_scale;
-    t.topk_idx = h->buf<int>(MONO_BUF_TOPK_IDX);
-    t.topk_w = h->buf<float>(MONO_BUF_TOPK_W);
-    t.slot_pos = h->buf<int>(MONO_BUF_SLOT_POS);
-    t.perm = h->perm;
-    t.route = h->route;
-    t.user_idx = a->topk_idx_out;
-    t.user_w = a->topk_w_out;
-    t.status = h->status;
-    RUN(launch_topk(L, t));
-  }
-  // Large steps: the persistent expert GEMM starts right after the top-k and the shared
-  // expert joins before the final combine.  Small steps: the routed experts' clusters want
-  // every SM at once (items are assigned statically), so they wait for the shared expert.
-  const bool late_join = fork && R * K > EXPERT_SMALL_SLOTS;
-  if (fork && !late_join) {
-    RUN_PLAIN(cudaStreamWaitEvent(stream, h->ev_join, 0));
-  } else if (!fork) {
-    const int rs = shared_expert();
-    if (rs != MONO_OK) return rs;
-  }
-  RUN(expert(h->map_ex_gu, h->w.ex_gu_s, H, 2 * s.moe_inter, s.moe_inter, s.moe_inter / BOX_ROWS,
-             h->buf<__half>(MONO_BUF_U), H, h->perm, EPI_SWIGLU_F16, h->buf<void>(MONO_BUF_TR),
-             s.moe_inter));
-  RUN(expert(h->map_ex_d, h->w.ex_d_s, s.moe_inter, H, 0, H / TILE_M, h->buf<__half>(MONO_BUF_TR),
-             s.moe_inter, nullptr, EPI_F32, h->buf<void>(MONO_BUF_YR), H));
-  if (late_join) RUN_PLAIN(cudaStreamWaitEvent(stream, h->ev_join, 0));
-  {
-    FinalArgs f = {};
-    f.x = x;
-    f.h = h->buf<__nv_bfloat16>(MONO_BUF_H);
-    f.ys = h->buf<float>(MONO_BUF_YS);
-    f.yr = h->buf<float>(MONO_BUF_YR);
-    f.slot_pos = h->buf<int>(MONO_BUF_SLOT_POS);
-    f.topk_w = h->buf<float>(MONO_BUF_TOPK_W);
-    f.positions = a->positions;
-    f.rows = R;
-    f.H = H;
-    f.k = K;
-    f.out = reinterpret_cast<__nv_bfloat16*>(a->x_out);
-    RUN(launch_final(L, f));
-  }
-#undef RUN
-#undef RUN_PLAIN
-  if (h->profiling) {
-    e = cudaEventRecord(h->prof[kLaunchesPerStep], stream);
-    if (e != cudaSuccess) return cuda_fail(e);
-  }
-  return MONO_OK;
+  MoeIn m = {};
+  m.seam = {h->buf<__nv_bfloat16>(MONO_BUF_H), H, (const __nv_bfloat16*)h->w.ffn_norm, H, s.eps,
+            h->buf<__half>(MONO_BUF_U), H};
+  m.x = x;
+  m.positions = a->positions;
+  m.R = R;
+  m.topk_idx_out = a->topk_idx_out;
+  m.topk_w_out = a->topk_w_out;
+  m.x_out = a->x_out;
+  return enqueue_moe(h, m, run);
 }
+
+int mono_ffn_step(mono_layer_t* h, const mono_ffn_args* a, void* stream_ptr) {
+  if (!h || !a) return MONO_ERR_INVALID_ARG;
+  const mono_layer_spec& s = h->spec;
+  const int R = a->rows;
+  if (R < 1) return MONO_ERR_INVALID_ARG;
+  if (R > s.max_rows) return MONO_ERR_TOO_MANY_ROWS;
+  if (!a->x_in || !a->attn_in || !a->x_out || !a->positions) return MONO_ERR_INVALID_ARG;
+  if (!aligned16(a->x_in) || !aligned16(a->attn_in) || !aligned16(a->x_out))
+    return MONO_ERR_BAD_ALIGNMENT;
+  const cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+  Enqueue run{h, stream, kFfnFirstLaunch};
+  const int H = s.hidden;
+  MoeIn m = {};
+  m.seam = {reinterpret_cast<const __nv_bfloat16*>(a->x_in), H,
+            (const __nv_bfloat16*)h->w.ffn_norm, H, s.eps, h->buf<__half>(MONO_BUF_U), H,
+            reinterpret_cast<const __nv_bfloat16*>(a->attn_in), H,
+            h->buf<__nv_bfloat16>(MONO_BUF_H), H};
+  m.x = reinterpret_cast<const __nv_bfloat16*>(a->x_in);
+  m.positions = a->positions;
+  m.R = R;
+  m.topk_idx_out = a->topk_idx_out;
+  m.topk_w_out = a->topk_w_out;
+  m.x_out = a->x_out;
+  return enqueue_moe(h, m, run);
+}
+
+#undef TRY
+#undef TRY_CUDA
 
 }  // extern "C"

@@ -68,6 +68,39 @@ def run_step(layer, spec, sd, rows, x_out=None):
     return g
 
 
+def run_ffn_step(layer, spec, x, attn, positions, x_out=None):
+    """One FFN launch; returns host copies of its output and of the MoE-half buffers."""
+    dev = x.device
+    rows = x.shape[0]
+    out = torch.empty_like(x) if x_out is None else x_out
+    K = spec["topk"]
+    idx = torch.full((rows, K), -7, dtype=torch.int32, device=dev)
+    wts = torch.zeros((rows, K), dtype=torch.float32, device=dev)
+    layer.ffn_step(x, attn, out, positions, topk_idx_out=idx, topk_w_out=wts)
+    torch.cuda.synchronize()
+    H, E, I, Is = spec["hidden"], spec["n_experts"], spec["moe_inter"], spec["shared_inter"]
+
+    def rd(name, dtype, shape):
+        n = int(np.prod(shape)) * np.dtype(dtype).itemsize
+        return layer.read(name, n).view(dtype).reshape(shape)
+
+    return dict(
+        status=layer.status(),
+        out=out.cpu().view(torch.int16).numpy().view(np.uint16),
+        user_idx=idx.cpu().numpy(), user_w=wts.cpu().numpy(),
+        h=rd("h", np.uint16, (rows, H)),
+        u=f16_to_bf16_bits(rd("u", np.float16, (rows, H))),
+        logits=rd("logits", np.float32, (rows, E)),
+        topk_idx=rd("topk_idx", np.int32, (rows, K)),
+        topk_w=rd("topk_w", np.float32, (rows, K)),
+        slot_pos=rd("slot_pos", np.int32, (rows, K)),
+        t_s=f16_to_bf16_bits(rd("ts", np.float16, (rows, Is))),
+        y_s=rd("ys", np.float32, (rows, H)),
+        t_r=f16_to_bf16_bits(rd("tr", np.float16, (rows * K, I))),
+        y_r=rd("yr", np.float32, (rows * K, H)),
+    )
+
+
 def routed_sum(g):
     """sum_j w_j y_j per row from the GPU's buffers."""
     out = np.zeros(g["y_s"].shape, np.float64)
@@ -130,8 +163,17 @@ def check_stages(spec, wn, sn, g, rows):
     res["oa"] = bf16_ulp_check(g["oa"], _round(oracle.gemv_mxfp8(g["o"], wn["wo_a"], wn["wo_a_s"])), "oa")
     h_want = _round(bf16_f64(sn["x"]) + oracle.gemv_mxfp8(g["oa"], wn["wo_b"], wn["wo_b_s"]))
     res["h"] = bf16_ulp_check(g["h"], h_want, "h")
+    ties = check_moe(spec, wn, sn["x"], sn["positions"], g, res)
+    return res, ties
+
+
+def check_moe(spec, wn, x, positions, g, res):
+    """The FFN seam and MoE stages (u .. out) against the oracle stages on the GPU's own
+    inputs; returns the near-tie rows of the routing."""
+    valid = np.asarray(positions) >= 0
+    eps, K = spec["eps"], spec["topk"]
     res["u"] = bf16_ulp_check(g["u"], oracle.rmsnorm(g["h"], wn["ffn_norm"], eps), "u")
-    rt = oracle.router(g["u"], wn["router"], K, spec["routed_scale"], positions=sn["positions"])
+    rt = oracle.router(g["u"], wn["router"], K, spec["routed_scale"], positions=positions)
     res["logits"] = f32_check(g["logits"][valid], rt["logits"][valid], "logits", rel=1e-5)
     from tests.parity import topk_agree
     ok, ties = topk_agree(g["topk_idx"], rt["idx"], rt["probs"], K, valid)
@@ -170,10 +212,10 @@ def check_stages(spec, wn, sn, g, rows):
     res["y_r"] = f32_check(np.concatenate(yr_g), np.concatenate(yr_w), "y_r")
     # final combine
     out_want = _round(bf16_f64(g["h"]) + moe_sum(g))
-    out_want[~valid] = sn["x"][~valid]
+    out_want[~valid] = x[~valid]
     res["out"] = bf16_ulp_check(g["out"], out_want, "out")
-    assert np.array_equal(g["out"][~valid], sn["x"][~valid])
-    return res, ties
+    assert np.array_equal(g["out"][~valid], x[~valid])
+    return ties
 
 
 def oracle_threads():

@@ -45,6 +45,7 @@ def test_null_arguments_are_refused(built):
     h = C.c_void_p()
     assert built.mono_layer_build(None, None, C.byref(h)) == -1
     assert built.mono_layer_step(None, None, None) == -1
+    assert built.mono_ffn_step(None, None, None) == -1
     assert built.mono_layer_status(None, 0) == -1
     built.mono_layer_free(None)
 
@@ -74,6 +75,8 @@ int main(void) {
   printf("%zu %zu %zu\\n", sizeof(mono_layer_spec), sizeof(mono_layer_weights), sizeof(mono_step_args));
   printf("%zu %zu %zu %zu\\n", offsetof(mono_layer_spec, eps), offsetof(mono_step_args, rows),
          offsetof(mono_step_args, kv_cache), offsetof(mono_step_args, topk_w_out));
+  printf("%zu %zu %zu\\n", sizeof(mono_ffn_args), offsetof(mono_ffn_args, rows),
+         offsetof(mono_ffn_args, topk_w_out));
   return 0;
 }
 """)
@@ -81,5 +84,20 @@ int main(void) {
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
     got = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
     want = [C.sizeof(m.Spec), C.sizeof(m.Weights), C.sizeof(m.StepArgs), m.Spec.eps.offset,
-            m.StepArgs.rows.offset, m.StepArgs.kv_cache.offset, m.StepArgs.topk_w_out.offset]
+            m.StepArgs.rows.offset, m.StepArgs.kv_cache.offset, m.StepArgs.topk_w_out.offset,
+            C.sizeof(m.FfnArgs), m.FfnArgs.rows.offset, m.FfnArgs.topk_w_out.offset]
     assert [int(v) for v in got] == want
+
+
+def test_attention_weights_all_or_none(built):
+    import gen
+    spec = gen.spec_of("tiny", max_rows=1)
+    h = C.c_void_p()
+    half = {k: (None if k in ("wqkv", "wo_b_s") else 16 * (i + 1)) for i, k in enumerate(m.WEIGHT_FIELDS)}
+    assert built.mono_layer_build(C.byref(m.make_spec(spec)), C.byref(m.Weights(**half)), C.byref(h)) == -1
+    ffn = {k: (None if k in m.ATTN_WEIGHT_FIELDS else 16 * (i + 1)) for i, k in enumerate(m.WEIGHT_FIELDS)}
+    # an FFN-only handle still checks the FFN fields
+    bad = dict(spec, moe_inter=100)
+    assert built.mono_layer_build(C.byref(m.make_spec(bad)), C.byref(m.Weights(**ffn)), C.byref(h)) == -2
+    ffn["router"] = None
+    assert built.mono_layer_build(C.byref(m.make_spec(spec)), C.byref(m.Weights(**ffn)), C.byref(h)) == -1
