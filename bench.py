@@ -4,9 +4,11 @@ bandwidth it sustains, on synthetic seeded inputs.
 Headline workload: one full-size layer at 48 rows (8 requests x 6 rows, causal window 128,
 contexts uniform in [1024, 65536], 128 experts top-6), the configuration the 60%-of-HBM
 target is set on.  The same JSON line carries the 1-row and 6-row (draft, top-3,
-non-causal 192-wide rows) shapes under "rows_sweep", together with the stacked decode step
-(30 full-size 48-row layers with distinct weights and KV caches, each layer's output the
-next one's input, one CUDA graph: "stacked_30x48").
+non-causal 192-wide rows) shapes under "rows_sweep", together with the FFN launch alone at 6
+and 48 rows ("ffn_launch_r6", "ffn_launch_r48": the residual from an attention output, then
+the FFN seam and the MoE) and the stacked decode step (30 full-size 48-row layers with
+distinct weights and KV caches, each layer's output the next one's input, one CUDA graph:
+"stacked_30x48").
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -294,6 +296,69 @@ def measure_stacked(n_layers, steps, warmup, dev):
                 frac_of_measured_copy=None, d_hit_min=int(min(d_hit)), d_hit_max=int(max(d_hit)))
 
 
+def ffn_bytes(spec: dict, rows: int, d_hit: int) -> int:
+    """Algorithmic bytes of one FFN launch: the FFN-seam gamma, the router, the shared
+    expert, the hit experts, and the hidden rows (x and the attention output read, h
+    written, the output written)."""
+    wb = gen.weight_bytes(spec)
+    return (2 * spec["hidden"] + wb["router"] + wb["shared"] + d_hit * wb["expert"]
+            + 4 * rows * spec["hidden"] * 2)
+
+
+def measure_ffn(rows, steps, warmup, dev, n_copies):
+    """The FFN launch (residual from an attention output, then the FFN seam and the MoE) on
+    the first `rows` rows of the 48-row step (6 rows = one request of 6 tokens), on FFN-only
+    handles rotating over n_copies distinct weight sets, replayed from one CUDA graph."""
+    import moe_decode_layer_mxfp8_gb300 as m
+    name = "full_r48"
+    wl = gen.WORKLOADS[name]
+    spec = gen.spec_of(name)
+    step = gen.make_step(spec, wl, device=dev)
+    spec["max_rows"] = rows
+    x = step["x"][:rows].contiguous()
+    pos = step["positions"][:rows].contiguous()
+    a = gen.make_attn_out(spec, step, seed=wl["seed"], device=dev)[:rows].contiguous()
+    layers = []
+    for c in range(n_copies):
+        w = gen.make_weights(spec, wl["seed"] + 1000 * c, device=dev)
+        w = {k: v for k, v in w.items() if k not in m.ATTN_WEIGHT_FIELDS}
+        layers.append(m.Layer(spec, w))
+    outs = [torch.empty_like(x) for _ in layers]
+    stream = torch.cuda.Stream(dev)
+    idx = torch.empty((rows, spec["topk"]), dtype=torch.int32, device=dev)
+    d_hit = []
+    with torch.cuda.stream(stream):
+        for c, lay in enumerate(layers):
+            lay.ffn_step(x, a, outs[c], pos, stream=stream, topk_idx_out=idx)
+            stream.synchronize()
+            d_hit.append(len(np.unique(idx.cpu().numpy())))
+            assert lay.status() == 0
+        n_graph = len(layers) * max(1, 64 // len(layers))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n_graph):
+                layers[i % len(layers)].ffn_step(x, a, outs[i % len(layers)], pos, stream=stream)
+        for _ in range(max(3, warmup)):
+            g.replay()
+    torch.cuda.synchronize(dev)
+    reps = max(1, steps // n_graph)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        t1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = t0.elapsed_time(t1) * 1000.0 / (reps * n_graph)
+    byts = float(np.mean([ffn_bytes(spec, rows, d) for d in d_hit]))
+    for lay in layers:
+        lay.close()
+    del layers, g
+    torch.cuda.empty_cache()
+    return dict(rows=rows, us_per_launch=round(us, 2), hbm_gbs=round(byts / us / 1e3, 1),
+                bytes_per_launch=int(byts), d_hit=d_hit, copies=n_copies)
+
+
 def kernel_profile(res, dev, reps=20):
     """Per-launch CUDA-event times (eager steps, programmatic overlap off while profiling)."""
     spec, step, layers, stream = res["spec"], res["step"], res["layers"], res["stream"]
@@ -532,6 +597,11 @@ def main():
                                    bytes_per_step=int(r["bytes"]), d_hit=r["d_hit"])
                 del r
                 torch.cuda.empty_cache()
+            # the FFN launch alone at one request x 6 tokens and at 8 requests x 6 tokens
+            for r_ffn in (6, 48):
+                f = measure_ffn(r_ffn, 1000, args.warmup, dev, 2 if r_ffn == 48 else 3)
+                f["frac_of_measured_copy"] = round(f["hbm_gbs"] / peak, 4)
+                sweep[f"ffn_launch_r{r_ffn}"] = f
             # configuration 5: 30 stacked 48-row layers, one graph, residual carried
             stacked = measure_stacked(STACKED_LAYERS, 20, args.warmup, dev)
             stacked["frac_of_measured_copy"] = round(stacked["hbm_gbs"] / peak, 4)
