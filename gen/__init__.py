@@ -26,6 +26,8 @@ MXFP4 routed experts with 1x32 scales):
 * ``draft_r6``    as full but top-3, non-causal rows 192 wide, context 65536, the
                   same hidden vector repeated to 6 rows.
 * ``full_r48``    as full, 8 requests x 6 rows, contexts uniform in [1024, 65536].
+* ``draft_r48``   the draft shape with one request of 48 identical rows: every row routes
+                  to the same 3 experts.
 """
 from __future__ import annotations
 
@@ -58,6 +60,10 @@ WORKLOADS = {
                      rows_per_req=6, pad_rows=0, seed=2, repeat_input=True),
     "full_r48": dict(spec=_FULL, contexts="uniform:1024:65536:8", rows_per_req=6,
                      pad_rows=0, seed=3),
+    # every row identical in one non-causal request: all 48 rows route to the same 3
+    # experts (48 routed rows per expert, the most concentrated routing a step can have)
+    "draft_r48": dict(spec=dict(_FULL, topk=3, causal=0, swa_width=192), contexts=[40000],
+                      rows_per_req=48, pad_rows=0, seed=15, repeat_input=True),
     # parity-only shapes that reach the remaining code paths: 4 one-token requests (a small
     # step whose many expert items do not split K), 24 rows (the 4-tile dense variant), and a
     # narrow layer with 256 experts, top-8, head_dim 64 and a 300-token window (3 splits)

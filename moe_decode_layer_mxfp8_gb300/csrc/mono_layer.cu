@@ -493,35 +493,14 @@ int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
   TRY(run([&] {
     return launch_router(L, {h->buf<__half>(MONO_BUF_U), h->w.router, R, E, H, h->router_part});
   }));
-  // The shared expert depends only on u: fork it onto the side stream after the router (whose
-  // CTAs are then resident before the shared expert's GEMM CTAs claim the SMs) so that it
-  // overlaps the top-k (and, in large steps, the routed experts).  While profiling,
+  // The shared expert depends only on u: it runs on the side stream, forked after the router,
+  // so that it overlaps the top-k and, in large steps, the routed experts.  The top-k is
+  // launched first: its one CTA then takes an SM (it asks for most of one, so that no GEMM CTA
+  // shares it) before the shared expert's GEMM CTAs fill the GPU.  While profiling,
   // everything stays on one stream in launch-name order.
   const bool fork = !h->profiling;
   const Launch Ls{fork ? h->side : stream, !h->profiling};
-  if (fork) {
-    TRY_CUDA(cudaEventRecord(h->ev_fork, stream));
-    TRY_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
-  }
-  auto shared_expert = [&]() -> int {
-    TRY(run([&] {
-      return dense_launch(h, D_SHGU, R, h->buf<__half>(MONO_BUF_U), H, EPI_SWIGLU_F16,
-                          h->buf<void>(MONO_BUF_TS), s.shared_inter, nullptr, Ls);
-    }));
-    TRY(run([&] {
-      return dense_launch(h, D_SHD, R, h->buf<__half>(MONO_BUF_TS), s.shared_inter, EPI_F32,
-                          h->buf<void>(MONO_BUF_YS), H, nullptr, Ls);
-    }));
-    return MONO_OK;
-  };
-  // launch indices stay in name order although the shared expert is enqueued first
-  const int topk_no = run.next;
-  if (fork) {
-    run.next = topk_no + 1;
-    TRY(shared_expert());
-    TRY_CUDA(cudaEventRecord(h->ev_join, h->side));
-    run.next = topk_no;
-  }
+  if (fork) TRY_CUDA(cudaEventRecord(h->ev_fork, stream));
   {
     TopkArgs t = {};
     t.partial = h->router_part;
@@ -542,16 +521,21 @@ int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
     t.status = h->status;
     TRY(run([&] { return launch_topk(L, t); }));
   }
+  if (fork) TRY_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
+  TRY(run([&] {
+    return dense_launch(h, D_SHGU, R, h->buf<__half>(MONO_BUF_U), H, EPI_SWIGLU_F16,
+                        h->buf<void>(MONO_BUF_TS), s.shared_inter, nullptr, Ls);
+  }));
+  TRY(run([&] {
+    return dense_launch(h, D_SHD, R, h->buf<__half>(MONO_BUF_TS), s.shared_inter, EPI_F32,
+                        h->buf<void>(MONO_BUF_YS), H, nullptr, Ls);
+  }));
+  if (fork) TRY_CUDA(cudaEventRecord(h->ev_join, h->side));
   // Large steps: the persistent expert GEMM starts right after the top-k and the shared
   // expert joins before the final combine.  Small steps: the routed experts' clusters want
   // every SM at once (items are assigned statically), so they wait for the shared expert.
   const bool late_join = fork && R * K > EXPERT_SMALL_SLOTS;
-  if (fork) {
-    run.next += 2;
-    if (!late_join) TRY_CUDA(cudaStreamWaitEvent(stream, h->ev_join, 0));
-  } else {
-    TRY(shared_expert());
-  }
+  if (fork && !late_join) TRY_CUDA(cudaStreamWaitEvent(stream, h->ev_join, 0));
   TRY(run([&] {
     return expert_launch(h, R, h->map_ex_gu, h->w.ex_gu_s, H, 2 * s.moe_inter, s.moe_inter,
                          s.moe_inter / BOX_ROWS, h->buf<__half>(MONO_BUF_U), H, h->perm,

@@ -20,7 +20,8 @@ from tests.parity import layer_metrics, layer_ok, near_tie_rows
 
 pytestmark = pytest.mark.gpu
 
-WORKLOADS = ["tiny", "small_r11", "wide_r9", "full_r1", "full_r4", "draft_r6", "full_r24", "full_r48"]
+WORKLOADS = ["tiny", "small_r11", "wide_r9", "full_r1", "full_r4", "draft_r6", "full_r24", "full_r48",
+             "draft_r48"]
 _cache = {}
 
 
@@ -77,6 +78,12 @@ def test_layer_matches_oracle(name):
     assert layer_ok(m), m
     assert np.array_equal(g["cache"], ref["cache"]) or name.startswith("full") or name == "draft_r6" \
         or (g["cache"] != ref["cache"]).sum() <= 8 * spec["kv_dim"]
+
+
+def test_draft_r48_concentrates_every_row_on_three_experts():
+    spec, wn, sn, g, *_ = _case("draft_r48")
+    assert (g["topk_idx"] == g["topk_idx"][0]).all()
+    assert len(np.unique(g["topk_idx"])) == 3
 
 
 def test_full_r48_routes_at_least_60_experts():
