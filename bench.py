@@ -16,7 +16,8 @@ distinct weights and KV caches, each layer's output the next one's input, one CU
   resident in HBM; the layer's weights rotate over several distinct copies so that no step
   finds its weights in L2.
 * e2e: the same step through the public C ABI from pinned host buffers (inputs copied in,
-  output copied out, every step).
+  output copied out, every step; the copies run on a second stream, overlapping the
+  neighbouring steps' compute).
 * roofline: the dominant kernel's algorithmic bytes per launch over its CUDA-event time.
 * cpu_baseline: the CPU oracle on the host cores (a reported baseline only).
 * --impl reference: the oracle, timed as it stands, is the reference arm.
@@ -388,43 +389,72 @@ def kernel_profile(res, dev, reps=20):
 
 
 def measure_e2e(res, steps, warmup, dev):
-    """Public API with host buffers: pinned inputs copied in and the output copied out
-    every step, all inside the timed region."""
+    """Public API with host buffers: every step's inputs are copied in from pinned host memory
+    and its output copied back out, all inside the timed region.  The copies run on a copy
+    stream with two sets of device buffers, so that step i + 1's inputs arrive and step
+    i - 1's output leaves while step i computes (each step's copies still bracket its own
+    compute)."""
     spec, step, layers = res["spec"], res["step"], res["layers"]
     stream = res["stream"]
+    copy = torch.cuda.Stream(dev)
     rows, H = step["rows"], spec["hidden"]
-    h_x = step["x"].cpu().pin_memory()
-    h_pos = step["positions"].cpu().pin_memory()
-    h_req = step["row_req"].cpu().pin_memory()
-    h_tab = step["block_table"].cpu().pin_memory()
-    h_out = torch.empty((rows, H), dtype=torch.bfloat16).pin_memory()
-    d_x = torch.empty_like(step["x"])
-    d_pos, d_req, d_tab = (torch.empty_like(step[k]) for k in ("positions", "row_req", "block_table"))
-    d_out = torch.empty_like(step["x"])
+    h_in = {k: step[k].cpu().pin_memory() for k in ("x", "positions", "row_req", "block_table")}
+    h_out = [torch.empty((rows, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    d_in = [{k: torch.empty_like(step[k]) for k in h_in} for _ in range(2)]
+    d_out = [torch.empty_like(step["x"]) for _ in range(2)]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
 
-    def one(i):
+    def h2d(i):
+        b = i % 2
+        with torch.cuda.stream(copy):
+            if used[b]:  # step i - 2 has finished reading these inputs
+                copy.wait_event(ev_done[b])
+            for k, t in h_in.items():
+                d_in[b][k].copy_(t, non_blocking=True)
+            ev_in[b].record(copy)
+
+    def compute(i):
+        b = i % 2
         lay, _ = layers[i % len(layers)]
-        d_x.copy_(h_x, non_blocking=True)
-        d_pos.copy_(h_pos, non_blocking=True)
-        d_req.copy_(h_req, non_blocking=True)
-        d_tab.copy_(h_tab, non_blocking=True)
-        lay.step(d_x, d_out, d_pos, d_req, d_tab, step["kv_cache"], stream=stream)
-        h_out.copy_(d_out, non_blocking=True)
+        with torch.cuda.stream(stream):
+            stream.wait_event(ev_in[b])
+            if used[b]:  # step i - 2's output has left this buffer
+                stream.wait_event(ev_out[b])
+            d = d_in[b]
+            lay.step(d["x"], d_out[b], d["positions"], d["row_req"], d["block_table"],
+                     step["kv_cache"], stream=stream)
+            ev_done[b].record(stream)
+        used[b] = True
 
-    with torch.cuda.stream(stream):
-        for i in range(max(3, warmup)):
-            one(i)
-        stream.synchronize()
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for i in range(steps):
-            one(i)
-        t1.record(stream)
+    def d2h(i):
+        b = i % 2
+        with torch.cuda.stream(copy):
+            copy.wait_event(ev_done[b])
+            h_out[b].copy_(d_out[b], non_blocking=True)
+            ev_out[b].record(copy)
+
+    def run(n):
+        h2d(0)
+        for i in range(n):
+            if i + 1 < n:
+                h2d(i + 1)
+            compute(i)
+            d2h(i)
+
+    run(max(3, warmup))
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(copy)
+    run(steps)
+    t1.record(copy)
     torch.cuda.synchronize(dev)
     us = t0.elapsed_time(t1) * 1000.0 / steps
-    h2d = sum(t.numel() * t.element_size() for t in (h_x, h_pos, h_req, h_tab))
-    d2h = h_out.numel() * h_out.element_size()
-    return dict(value=us, unit=UNIT, h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(d2h))
+    h2d_b = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h_b = h_out[0].numel() * h_out[0].element_size()
+    return dict(value=us, unit=UNIT, h2d_bytes_per_step=int(h2d_b), d2h_bytes_per_step=int(d2h_b))
 
 
 def cpu_baseline(res):
