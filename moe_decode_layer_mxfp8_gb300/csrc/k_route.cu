@@ -2,9 +2,9 @@
 // table K2: "router, top-6"; ATOM changes: "f32 router logits").
 //
 // router_kernel: z[r, e] = u[r] . W_r[e] in f32, split over K: CTA (4 experts x 2 warps,
-// 1024-wide K slice) holds its experts' weight slices in registers (fetched before waiting on the
-// previous kernel), stages the slice of every row of u in shared memory and writes one
-// partial per (slice, row, expert).  Rows go eight at a time: eight independent FMA chains
+// 1024-wide K slice, 16 rows) holds its experts' weight slices in registers (fetched before
+// waiting on the previous kernel), stages the slice of its rows of u in shared memory and
+// writes one partial per (slice, row, expert).  Rows go eight at a time: eight independent FMA chains
 // per lane, then one transposing butterfly that leaves each of eight lanes with one row's
 // sum.
 //
@@ -24,6 +24,7 @@ constexpr int RT_EXPERTS = 4;    // experts per CTA
 constexpr int RT_HALVES = 2;     // warps per expert, taking alternate groups of 8 rows
 constexpr int RT_THREADS = RT_EXPERTS * RT_HALVES * 32;
 constexpr int RT_J = ROUTER_KSLICE / 128;  // float4 weight chunks per lane
+constexpr int RT_ROWS = 8 * RT_HALVES;     // rows per CTA (grid z = row groups)
 constexpr int MAX_ROWS = 48, MAX_K = 8;
 
 __global__ void __launch_bounds__(RT_THREADS) router_kernel(RouterArgs a) {
@@ -43,21 +44,24 @@ __global__ void __launch_bounds__(RT_THREADS) router_kernel(RouterArgs a) {
                 ? *reinterpret_cast<const float4*>(a.wr + (size_t)e * a.H + k0 + 128 * j + 4 * lane)
                 : make_float4(0.f, 0.f, 0.f, 0.f);
   pdl_wait();
+  // this CTA's rows [row0, row0 + nrows)
+  const int row0 = blockIdx.z * RT_ROWS;
+  const int nrows = min(RT_ROWS, a.rows - row0);
   const int chunks = klen / 8;  // 16-byte chunks per row
-  for (int idx = tid; idx < a.rows * chunks; idx += RT_THREADS) {
+  for (int idx = tid; idx < nrows * chunks; idx += RT_THREADS) {
     const int r = idx / chunks, c = idx - r * chunks;
-    cp_async16(us + r * ROUTER_KSLICE + c * 8, a.u + (size_t)r * a.H + k0 + c * 8, 16);
+    cp_async16(us + r * ROUTER_KSLICE + c * 8, a.u + (size_t)(row0 + r) * a.H + k0 + c * 8, 16);
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
   if (e >= a.E) return;
   // lane l ends a group of eight rows with the sum of row 4 bit4(l) + 2 bit3(l) + bit2(l)
   const int my_row = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-  for (int r0 = 8 * half; r0 < a.rows; r0 += 8 * RT_HALVES) {
+  for (int r0 = 8 * half; r0 < nrows; r0 += 8 * RT_HALVES) {
     float acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-    const int nr = min(8, a.rows - r0);
+    const int nr = min(8, nrows - r0);
 #pragma unroll
     for (int j = 0; j < RT_J; ++j) {
       if (128 * j < klen) {
@@ -96,8 +100,8 @@ __global__ void __launch_bounds__(RT_THREADS) router_kernel(RouterArgs a) {
     float v = (b2 ? s3[1] : s3[0]) + __shfl_xor_sync(0xffffffffu, b2 ? s3[0] : s3[1], 4);
     v += __shfl_xor_sync(0xffffffffu, v, 2);
     v += __shfl_xor_sync(0xffffffffu, v, 1);
-    if ((lane & 3) == 0 && r0 + my_row < a.rows)
-      a.partial[((size_t)blockIdx.y * a.rows + r0 + my_row) * a.E + e] = v;
+    if ((lane & 3) == 0 && r0 + my_row < nrows)
+      a.partial[((size_t)blockIdx.y * a.rows + row0 + r0 + my_row) * a.E + e] = v;
   }
 }
 
@@ -276,7 +280,7 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
 
 }  // namespace
 
-int router_smem_bytes(int rows) { return rows * ROUTER_KSLICE * 2; }
+int router_smem_bytes() { return RT_ROWS * ROUTER_KSLICE * 2; }
 // The logits of the step in shared memory, [rows][E].
 // The kernel is one latency-bound CTA: it asks for more shared memory than its logits need
 // (200 KB) so that no GEMM CTA of the concurrently running shared expert lands on its SM and
@@ -289,7 +293,7 @@ int topk_smem_bytes() { return TOPK_SMEM; }
 // them for the largest step any handle accepts.
 cudaError_t router_prepare() {
   cudaError_t e = cudaFuncSetAttribute(router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       router_smem_bytes(MAX_ROWS));
+                                       router_smem_bytes());
   if (e != cudaSuccess) return e;
   for (auto k : {topk_kernel<1>, topk_kernel<2>, topk_kernel<4>, topk_kernel<8>}) {
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, topk_smem_bytes());
@@ -299,8 +303,9 @@ cudaError_t router_prepare() {
 }
 
 cudaError_t launch_router(const Launch& L, const RouterArgs& a) {
-  const dim3 grid((a.E + RT_EXPERTS - 1) / RT_EXPERTS, (a.H + ROUTER_KSLICE - 1) / ROUTER_KSLICE);
-  return launch_ex(L, grid, dim3(RT_THREADS), router_smem_bytes(a.rows), router_kernel, a);
+  const dim3 grid((a.E + RT_EXPERTS - 1) / RT_EXPERTS, (a.H + ROUTER_KSLICE - 1) / ROUTER_KSLICE,
+                  (a.rows + RT_ROWS - 1) / RT_ROWS);
+  return launch_ex(L, grid, dim3(RT_THREADS), router_smem_bytes(), router_kernel, a);
 }
 
 cudaError_t launch_topk(const Launch& L, const TopkArgs& a) {
