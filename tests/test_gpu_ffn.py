@@ -166,3 +166,15 @@ def test_layer_and_ffn_launch_in_one_graph_replay_bit_exactly():
     assert lay.status() == 0 and ffn.status() == 0
     assert torch.isfinite(bufs[3].float()).all()
     lay.close(), ffn.close()
+
+
+@pytest.mark.parametrize("alias", ["x_in", "attn_in"])
+def test_ffn_output_may_alias_an_input(alias):
+    _need_gpu()
+    spec, wn, sn, an, g, layer, wd, sd, ad = _case("small_r11")
+    x, a = sd["x"].clone(), ad.clone()
+    out = x if alias == "x_in" else a
+    layer.ffn_step(x, a, out, sd["positions"])
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert np.array_equal(_bits(out), g["out"])

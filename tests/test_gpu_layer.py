@@ -177,3 +177,15 @@ def test_handles_with_different_max_rows_coexist():
     assert layer.status() == 0
     assert np.array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), g["out"])
     small.close()
+
+
+def test_step_in_place_equals_out_of_place():
+    """x_out may alias x_in: the layer reads x (norm, residual, pad rows) before the final
+    combine overwrites it."""
+    _need_gpu()
+    spec, wn, sn, g, layer, wd, sd = _case("small_r11")
+    x = sd["x"].clone()
+    layer.step(x, x, sd["positions"], sd["row_req"], sd["block_table"], sd["kv_cache"].clone())
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert np.array_equal(x.cpu().view(torch.int16).numpy().view(np.uint16), g["out"])
