@@ -632,7 +632,7 @@ def main():
                 f = measure_ffn(r_ffn, 1000, args.warmup, dev, 2 if r_ffn == 48 else 3)
                 f["frac_of_measured_copy"] = round(f["hbm_gbs"] / peak, 4)
                 sweep[f"ffn_launch_r{r_ffn}"] = f
-            # configuration 5: 30 stacked 48-row layers, one graph, residual carried
+            # the stacked decode step: 30 full-size 48-row layers, one graph, residual carried
             stacked = measure_stacked(STACKED_LAYERS, 20, args.warmup, dev)
             stacked["frac_of_measured_copy"] = round(stacked["hbm_gbs"] / peak, 4)
             sweep["stacked_30x48"] = stacked
