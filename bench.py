@@ -159,6 +159,17 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------------------------ ranks
+def max_over_ranks(value: float, device) -> float:
+    """The largest value over the ranks of the initialised process group (a job's time is
+    its slowest replica's); the value itself when there is no process group."""
+    if not torch.distributed.is_initialized():
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------------------------ our arm
 def _layer_copies(name, n_copies, dev, seed0=None):
     import moe_decode_layer_mxfp8_gb300 as m
@@ -224,11 +235,8 @@ def measure_device(name, steps, warmup, dev, n_copies, sampler=None):
         run(steps)
         t1.record(stream)
     torch.cuda.synchronize(dev)
-    ms = t0.elapsed_time(t1)
+    ms = max_over_ranks(t0.elapsed_time(t1), dev)
     if torch.distributed.is_initialized():
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
         torch.distributed.barrier()
     us = ms * 1000.0 / steps
     # bytes per step averaged over the rotation actually run
