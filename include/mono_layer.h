@@ -185,6 +185,13 @@ int mono_ffn_step(mono_layer_t *h, const mono_ffn_args *args, void *stream);
  * word when `clear` is non-zero. */
 int mono_layer_status(mono_layer_t *h, int clear);
 
+/* Failure-path check: enqueues one thread that waits, through the same bounded mbarrier wait
+ * the pipelines use, on a barrier that nothing completes.  After budget_ns (1 us .. 1 s) the
+ * wait gives up, raises MONO_STATUS_WAIT_TIMEOUT in the handle's status word and the kernel
+ * returns normally, so the context stays usable.  MONO_ERR_INVALID_ARG for a budget out of
+ * range. */
+int mono_layer_selftest_wait_timeout(mono_layer_t *h, int64_t budget_ns, void *stream);
+
 /* Releases the handle's scratch arena and status word.  NULL is accepted. */
 void mono_layer_free(mono_layer_t *h);
 

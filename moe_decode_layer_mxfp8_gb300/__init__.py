@@ -62,7 +62,8 @@ EXPORTS = ["mono_layer_build", "mono_layer_step", "mono_ffn_step", "mono_layer_s
            "mono_layer_free",
            "mono_layer_strerror", "mono_layer_buffer", "mono_layer_read_buffer",
            "mono_layer_launches_per_step", "mono_layer_launch_name",
-           "mono_layer_set_profile_events", "mono_attention_noalloc"]
+           "mono_layer_set_profile_events", "mono_attention_noalloc",
+           "mono_layer_selftest_wait_timeout"]
 
 _lib = None
 
@@ -96,6 +97,7 @@ def lib() -> C.CDLL:
         L.mono_layer_launch_name.argtypes = [C.c_int]
         L.mono_layer_launch_name.restype = C.c_char_p
         L.mono_layer_set_profile_events.argtypes = [C.c_void_p, C.c_void_p, C.c_int]
+        L.mono_layer_selftest_wait_timeout.argtypes = [C.c_void_p, C.c_int64, C.c_void_p]
         _lib = L
     return _lib
 
@@ -175,6 +177,15 @@ class Layer:
         rc = lib().mono_ffn_step(self._h, C.byref(args), C.c_void_p(stream_handle))
         if rc != MONO_OK:
             raise MonoError(rc, "mono_ffn_step")
+
+    def selftest_wait_timeout(self, budget_ns: int, stream=None) -> None:
+        """Enqueues a bounded wait that runs out (the status word's WAIT_TIMEOUT bit)."""
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        rc = lib().mono_layer_selftest_wait_timeout(self._h, int(budget_ns), C.c_void_p(stream.cuda_stream))
+        if rc != MONO_OK:
+            raise MonoError(rc, "mono_layer_selftest_wait_timeout")
 
     def status(self, clear: bool = False) -> int:
         rc = lib().mono_layer_status(self._h, int(clear))

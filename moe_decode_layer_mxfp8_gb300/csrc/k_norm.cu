@@ -265,4 +265,18 @@ cudaError_t launch_final(const Launch& L, const FinalArgs& a) {
   return launch_ex(L, dim3(a.rows, ychunks), dim3(FINAL_THREADS), 0, final_kernel, a);
 }
 
+// One thread waits, through the pipelines' bounded mbarrier wait, on a barrier that nothing
+// completes: the wait gives up after budget_ns, raises ST_WAIT_TIMEOUT and the kernel returns.
+__global__ void wait_timeout_kernel(int* status, unsigned long long budget_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  (void)mbar_wait(&bar, 0, status, budget_ns);
+}
+
+cudaError_t launch_wait_timeout(cudaStream_t stream, int* status, unsigned long long budget_ns) {
+  wait_timeout_kernel<<<1, 1, 0, stream>>>(status, budget_ns);
+  return cudaGetLastError();
+}
+
 }  // namespace mono

@@ -125,6 +125,8 @@ cudaError_t launch_router(const Launch&, const RouterArgs&);
 cudaError_t router_prepare();  // raises the dynamic shared-memory limit
 cudaError_t launch_topk(const Launch&, const TopkArgs&);
 cudaError_t launch_final(const Launch&, const FinalArgs&);
+// A bounded wait that runs out (see mono_layer_selftest_wait_timeout).
+cudaError_t launch_wait_timeout(cudaStream_t stream, int* status, unsigned long long budget_ns);
 
 // MX GEMM variants: fmt 8 (MXFP8) with nt in {1, 2, 4, 6}; fmt 4 (MXFP4) with nt 1.
 struct GemmVariant {

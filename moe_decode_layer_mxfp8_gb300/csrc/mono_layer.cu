@@ -341,6 +341,13 @@ int mono_layer_status(mono_layer_t* h, int clear) {
   return v;
 }
 
+int mono_layer_selftest_wait_timeout(mono_layer_t* h, int64_t budget_ns, void* stream) {
+  if (!h || budget_ns < 1000 || budget_ns > 1000000000) return MONO_ERR_INVALID_ARG;
+  const cudaError_t e = launch_wait_timeout(reinterpret_cast<cudaStream_t>(stream), h->status,
+                                            (unsigned long long)budget_ns);
+  return e == cudaSuccess ? MONO_OK : cuda_fail(e);
+}
+
 int mono_layer_buffer(mono_layer_t* h, int which, void** dev_ptr, size_t* bytes) {
   if (!h || which < 0 || which >= MONO_BUF_COUNT) return MONO_ERR_INVALID_ARG;
   if (dev_ptr) *dev_ptr = h->arena + h->buf_off[which];

@@ -46,6 +46,7 @@ def test_null_arguments_are_refused(built):
     assert built.mono_layer_build(None, None, C.byref(h)) == -1
     assert built.mono_layer_step(None, None, None) == -1
     assert built.mono_ffn_step(None, None, None) == -1
+    assert built.mono_layer_selftest_wait_timeout(None, 1000000, None) == -1
     assert built.mono_layer_status(None, 0) == -1
     built.mono_layer_free(None)
 

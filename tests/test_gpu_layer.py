@@ -189,3 +189,23 @@ def test_step_in_place_equals_out_of_place():
     torch.cuda.synchronize()
     assert layer.status() == 0
     assert np.array_equal(x.cpu().view(torch.int16).numpy().view(np.uint16), g["out"])
+
+
+def test_wait_timeout_sets_status_and_leaves_the_context_usable():
+    """A bounded pipeline wait that runs out raises the status word's timeout bit and returns;
+    the next step runs normally."""
+    _need_gpu()
+    import moe_decode_layer_mxfp8_gb300 as m
+    spec, wn, sn, g, layer, wd, sd = _case("small_r11")
+    layer.status(clear=True)
+    layer.selftest_wait_timeout(2_000_000)  # 2 ms
+    torch.cuda.synchronize()
+    assert layer.status(clear=True) & m.STATUS_WAIT_TIMEOUT
+    assert layer.status() == 0
+    out = torch.empty_like(sd["x"])
+    layer.step(sd["x"], out, sd["positions"], sd["row_req"], sd["block_table"], sd["kv_cache"].clone())
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert np.array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), g["out"])
+    with pytest.raises(m.MonoError):
+        layer.selftest_wait_timeout(10)  # budget out of range
