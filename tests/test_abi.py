@@ -4,6 +4,7 @@ import ctypes as C
 import os
 import re
 import subprocess
+import sys
 
 import pytest
 
@@ -102,3 +103,20 @@ def test_attention_weights_all_or_none(built):
     assert built.mono_layer_build(C.byref(m.make_spec(bad)), C.byref(m.Weights(**ffn)), C.byref(h)) == -2
     ffn["router"] = None
     assert built.mono_layer_build(C.byref(m.make_spec(spec)), C.byref(m.Weights(**ffn)), C.byref(h)) == -1
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """No fallback: without libmono_layer.so the binding raises instead of computing anything."""
+    code = f"""
+import sys
+sys.path.insert(0, {ROOT!r})
+import moe_decode_layer_mxfp8_gb300 as m
+m.LIB_PATH = {str(tmp_path / 'absent.so')!r}
+try:
+    m.lib()
+except RuntimeError as e:
+    assert 'no CPU fallback' in str(e)
+    print('raised')
+"""
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True)
+    assert out.stdout.strip() == "raised", out.stderr
