@@ -180,3 +180,36 @@ def test_ffn_output_may_alias_an_input(alias):
     torch.cuda.synchronize()
     assert layer.status() == 0
     assert np.array_equal(_bits(out), g["out"])
+
+
+def test_empty_ffn_launch_is_refused():
+    _need_gpu()
+    import moe_decode_layer_mxfp8_gb300 as m
+    spec, wn, sn, an, g, layer, wd, sd, ad = _case("small_r11")
+    x = torch.zeros((0, spec["hidden"]), dtype=torch.bfloat16, device="cuda")
+    pos = torch.zeros(0, dtype=torch.int32, device="cuda")
+    with pytest.raises(m.MonoError) as e:
+        layer.ffn_step(x, x, x, pos)
+    assert e.value.code == -1
+    assert layer.status() == 0
+
+
+@pytest.mark.parametrize("name", ["small_r11", "full_r48"])
+def test_all_pad_ffn_launch_passes_x_through(name):
+    """Every row a pad row: the FFN launch returns x_in unchanged (the attention output is
+    not added on pad rows), routes to no expert and leaves the handle usable."""
+    spec, wn, sn, an, g, layer, wd, sd, ad = _case(name)
+    rows, K = sd["x"].shape[0], spec["topk"]
+    pos = torch.full_like(sd["positions"], -1)
+    out = torch.empty_like(sd["x"])
+    idx = torch.full((rows, K), -7, dtype=torch.int32, device="cuda")
+    wts = torch.full((rows, K), 5.0, dtype=torch.float32, device="cuda")
+    layer.ffn_step(sd["x"], ad, out, pos, topk_idx_out=idx, topk_w_out=wts)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert torch.equal(out.view(torch.int16), sd["x"].view(torch.int16))
+    assert (idx == -1).all() and (wts == 0).all()
+    layer.ffn_step(sd["x"], ad, out, sd["positions"])
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert np.array_equal(_bits(out), g["out"])

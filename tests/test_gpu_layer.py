@@ -209,3 +209,51 @@ def test_wait_timeout_sets_status_and_leaves_the_context_usable():
     assert np.array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), g["out"])
     with pytest.raises(m.MonoError):
         layer.selftest_wait_timeout(10)  # budget out of range
+
+
+def test_empty_step_is_refused_and_the_next_step_runs():
+    """rows = 0 is outside 1..max_rows: refused before any launch, nothing written."""
+    _need_gpu()
+    import moe_decode_layer_mxfp8_gb300 as m
+    spec, wn, sn, g, layer, wd, sd = _case("small_r11")
+    x = torch.zeros((0, spec["hidden"]), dtype=torch.bfloat16, device="cuda")
+    pos = torch.zeros(0, dtype=torch.int32, device="cuda")
+    cache = sd["kv_cache"].clone()
+    with pytest.raises(m.MonoError) as e:
+        layer.step(x, x, pos, pos, sd["block_table"], cache)
+    assert e.value.code == -1
+    torch.cuda.synchronize()
+    assert torch.equal(cache, sd["kv_cache"]) and layer.status() == 0
+    out = torch.empty_like(sd["x"])
+    layer.step(sd["x"], out, sd["positions"], sd["row_req"], sd["block_table"], cache)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert np.array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), g["out"])
+
+
+@pytest.mark.parametrize("name", ["small_r11", "full_r48"])
+def test_all_pad_rows_pass_x_through(name):
+    """The degenerate step: every row a pad row.  Pad rows leave the layer unchanged
+    (out = x, bit for bit), write no KV record and route to no expert (-1, weight 0), so the
+    expert GEMMs run with no work item (the clustered small-step and the persistent
+    large-step kernels alike)."""
+    spec, wn, sn, g, layer, wd, sd = _case(name)
+    rows, K = sd["x"].shape[0], spec["topk"]
+    pos = torch.full_like(sd["positions"], -1)
+    cache = sd["kv_cache"].clone()
+    out = torch.empty_like(sd["x"])
+    idx = torch.full((rows, K), -7, dtype=torch.int32, device="cuda")
+    wts = torch.full((rows, K), 5.0, dtype=torch.float32, device="cuda")
+    layer.step(sd["x"], out, pos, sd["row_req"], sd["block_table"], cache,
+               topk_idx_out=idx, topk_w_out=wts)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert torch.equal(out.view(torch.int16), sd["x"].view(torch.int16))
+    assert torch.equal(cache, sd["kv_cache"])
+    assert (idx == -1).all() and (wts == 0).all()
+    # and the handle's next real step is unaffected
+    out2 = torch.empty_like(sd["x"])
+    layer.step(sd["x"], out2, sd["positions"], sd["row_req"], sd["block_table"], cache)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert np.array_equal(out2.cpu().view(torch.int16).numpy().view(np.uint16), g["out"])
