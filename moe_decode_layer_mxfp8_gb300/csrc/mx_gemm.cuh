@@ -154,10 +154,15 @@ __device__ __forceinline__ void decode_item(const GemmParams& p, const RouteSmem
                                             int ks, Item& it) {
   constexpr int KC = FmtTraits<FMT>::KC;
   int base = 0;
-  it.split = q % ks;
-  q /= ks;
+  // every CTA's producer and consumer warps decode each of its items: the common cases (no K
+  // split, an expert with one row group) take no integer division
+  it.split = 0;
+  if (ks > 1) {
+    it.split = q % ks;
+    q /= ks;
+  }
   const int nck_all = (p.K + KC - 1) / KC;
-  const int cps = (nck_all + ks - 1) / ks;
+  const int cps = ks > 1 ? (nck_all + ks - 1) / ks : nck_all;
   const int c0 = it.split * cps;
   it.nck = max(0, min(cps, nck_all - c0));
   it.k0 = c0 * KC;
@@ -170,7 +175,7 @@ __device__ __forceinline__ void decode_item(const GemmParams& p, const RouteSmem
     const int d = lo;
     const int rgc = rs->rg_prefix[d + 1] - rs->rg_prefix[d];
     const int local = q - rs->rg_prefix[d] * p.n_tiles;
-    it.tile = local / rgc;
+    it.tile = rgc == 1 ? local : local / rgc;
     const int rg = local - it.tile * rgc;
     base = rs->hit_e[d] * p.rows_per_mat;
     it.n = min(EXPERT_ROWS, rs->hit_cnt[d] - rg * EXPERT_ROWS);
@@ -367,15 +372,14 @@ __device__ __forceinline__ float swiglu_clamped(float g, float u, float c) {
 }
 
 // Writes finished tile values to the output.  fin[m * EP_LD + i] holds the value of output
-// row (row0 + i), column (col0 + m) -- for SwiGLU tiles the already combined gate/up value --
-// for m in [m_lo, m_lo + per).  Four values per thread are in flight at a time, their
-// residual reads issued before any store.
-template <int EP_LD, int NTHR>
-__device__ void store_rows(const GemmParams& p, const Item& it, const float* fin, int m_lo,
-                           int per, int tid) {
+// row (row0 + i), column (col0 + m) -- for SwiGLU tiles (SW) the already combined gate/up
+// value -- for m in [0, per), per = 32 (SW) or 64 a compile-time constant.  Four values per
+// thread are in flight at a time, their residual reads issued before any store.
+template <int EP_LD, int NTHR, bool SW>
+__device__ void store_rows(const GemmParams& p, const Item& it, const float* fin, int tid) {
+  constexpr int per = SW ? BOX_ROWS : TILE_M;
   const int total = per * it.n;
-  const bool sw = p.epi == EPI_SWIGLU_F16;
-  const int ncols = sw ? p.swiglu_I : p.N;
+  const int ncols = SW ? p.swiglu_I : p.N;
   for (int base = tid; base < total; base += 4 * NTHR) {
     float v[4], r[4];
     size_t o[4];
@@ -383,7 +387,7 @@ __device__ void store_rows(const GemmParams& p, const Item& it, const float* fin
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int idx = base + u * NTHR;
-      const int i = idx / per, m = m_lo + (idx - (idx / per) * per);
+      const int i = idx / per, m = idx - (idx / per) * per;
       const int col = it.col0 + m;
       ok[u] = idx < total && col < ncols;
       o[u] = (size_t)(it.row0 + i) * p.out_ld + col;
@@ -426,7 +430,10 @@ __device__ void epilogue_local(const GemmParams& p, const Item& it, float* ep, i
     }
     consumer_bar<NTHR>();
   }
-  store_rows<EP_LD, NTHR>(p, it, ep, 0, sw ? BOX_ROWS : TILE_M, tid);
+  if (sw)
+    store_rows<EP_LD, NTHR, true>(p, it, ep, tid);
+  else
+    store_rows<EP_LD, NTHR, false>(p, it, ep, tid);
 }
 
 // owner_epilogue with the cluster size and the SwiGLU pairing as compile-time constants.
