@@ -52,13 +52,19 @@ struct RouteInfo {
   int rg_prefix[MAX_EXPERTS + 1];  // prefix sum of ceil(hit_cnt / EXPERT_ROWS)
 };
 
-// Shared-memory copy of the routing metadata plus the activation row map.
+// Shared-memory copy of the routing metadata plus the activation row map, and the hit
+// expert of every row group (expert d owns row groups [rg_prefix[d], rg_prefix[d + 1]) and
+// items [rg_prefix[d] * n_tiles, rg_prefix[d + 1] * n_tiles), so item q belongs to the
+// expert of row group q / n_tiles).
 struct RouteSmem {
   int n_hit;
+  int tile_shift;  // log2(n_tiles) when n_tiles is a power of two, else -1
   int hit_e[MAX_EXPERTS], hit_off[MAX_EXPERTS], hit_cnt[MAX_EXPERTS];
   int rg_prefix[MAX_EXPERTS + 1];
   int rowmap[MAX_SLOTS];
+  uint8_t rg_expert[MAX_SLOTS];  // row groups <= routed slots <= MAX_SLOTS
 };
+static_assert(MAX_EXPERTS <= 256, "rg_expert holds hit-expert indices in a byte");
 
 enum : int { EPI_BF16 = 0, EPI_F16 = 1, EPI_RESID_BF16 = 2, EPI_SWIGLU_F16 = 3, EPI_F32 = 4 };
 
@@ -167,12 +173,7 @@ __device__ __forceinline__ void decode_item(const GemmParams& p, const RouteSmem
   it.nck = max(0, min(cps, nck_all - c0));
   it.k0 = c0 * KC;
   if (rs) {
-    int lo = 0, hi = rs->n_hit - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (rs->rg_prefix[mid] * p.n_tiles <= q) lo = mid; else hi = mid - 1;
-    }
-    const int d = lo;
+    const int d = rs->rg_expert[rs->tile_shift >= 0 ? q >> rs->tile_shift : q / p.n_tiles];
     const int rgc = rs->rg_prefix[d + 1] - rs->rg_prefix[d];
     const int local = q - rs->rg_prefix[d] * p.n_tiles;
     it.tile = rgc == 1 ? local : local / rgc;
@@ -823,10 +824,17 @@ __global__ void __launch_bounds__(gemm_threads(KS), FMT == 4 && KS == 1 ? 4 : 2)
         rs->hit_cnt[i] = p.route->hit_cnt[i];
       }
       for (int i = threadIdx.x; i <= nh; i += THREADS) rs->rg_prefix[i] = p.route->rg_prefix[i];
+      for (int i = threadIdx.x; i < nh; i += THREADS) {
+        const int g1 = min(p.route->rg_prefix[i + 1], MAX_SLOTS);
+        for (int g = p.route->rg_prefix[i]; g < g1; ++g) rs->rg_expert[g] = (uint8_t)i;
+      }
       if (p.act_rowmap)
         for (int i = threadIdx.x; i < min(p.n_slots, MAX_SLOTS); i += THREADS)
           rs->rowmap[i] = p.act_rowmap[i];
-      if (threadIdx.x == 0) rs->n_hit = nh;
+      if (threadIdx.x == 0) {
+        rs->n_hit = nh;
+        rs->tile_shift = (p.n_tiles & (p.n_tiles - 1)) == 0 ? __ffs(p.n_tiles) - 1 : -1;
+      }
       __syncthreads();
     }
   }
