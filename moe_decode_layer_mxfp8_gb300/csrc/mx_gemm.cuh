@@ -437,6 +437,54 @@ __device__ void epilogue_local(const GemmParams& p, const Item& it, float* ep, i
     store_rows<EP_LD, NTHR, false>(p, it, ep, tid);
 }
 
+// One finished value of output row orow, column col, as store_rows writes it.
+__device__ __forceinline__ void store_value(const GemmParams& p, int orow, int col, float v) {
+  const size_t o = (size_t)orow * p.out_ld + col;
+  switch (p.epi) {
+    case EPI_BF16:
+      reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(v);
+      break;
+    case EPI_F16:
+    case EPI_SWIGLU_F16:
+      reinterpret_cast<__half*>(p.out)[o] = bf16_as_f16(v);
+      break;
+    case EPI_RESID_BF16:
+      reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(
+          __bfloat162float(p.resid[(size_t)orow * p.resid_ld + col]) + v);
+      break;
+    default:
+      reinterpret_cast<float*>(p.out)[o] = v;
+      break;
+  }
+}
+
+// Epilogue straight from the accumulators (large-step routed experts: one K share, no
+// cluster).  Thread (g, c) holds activation rows 8t + 2c and 8t + 2c + 1 of tile rows rowA
+// (acc[t][0..1]) and rowB (acc[t][2..3]); with pair_gu those are a gate row and its up row,
+// combined here into output column col0 + rowA.
+template <int NT>
+__device__ __forceinline__ void epilogue_regs(const GemmParams& p, const Item& it,
+                                              const float (&acc)[NT][4], int rowA, int rowB,
+                                              int c, bool pair_gu) {
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = 8 * t + 2 * c + h;
+      if (i >= it.n) continue;
+      if (pair_gu) {
+        const int col = it.col0 + rowA;
+        if (col < p.swiglu_I)
+          store_value(p, it.row0 + i, col, swiglu_clamped(acc[t][h], acc[t][2 + h], p.clamp));
+      } else {
+        const int ca = it.col0 + rowA, cb = it.col0 + rowB;
+        if (ca < p.N) store_value(p, it.row0 + i, ca, acc[t][h]);
+        if (cb < p.N) store_value(p, it.row0 + i, cb, acc[t][2 + h]);
+      }
+    }
+  }
+}
+
 // owner_epilogue with the cluster size and the SwiGLU pairing as compile-time constants.
 template <int EP_LD, int NTHR>
 __device__ __forceinline__ void owner_epilogue_any(const GemmParams& p, const Item& it,
@@ -599,7 +647,14 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
   const int w = tid >> 5, lane = tid & 31;
   const int mt = w & 3, kh = w >> 2;           // M-tile and K-half of this warp
   const int g = lane >> 2, c = lane & 3;
-  const int r0 = 16 * (mt & 1) + g;            // row of this thread inside its 32-row box
+  // tile rows of this thread's two MMA row halves (MMA rows g and g + 8).  Warp mt takes tile
+  // rows 16mt .. 16mt + 15, except in the large-step routed-expert kernel's SwiGLU tiles:
+  // there it takes gate rows 8mt .. 8mt + 7 with their up rows (the same rows of the second
+  // box), so that each thread holds a gate value and its up value and the epilogue needs no
+  // exchange between warps.  Both choices keep row & 7 = g, the 128-byte swizzle's key.
+  const bool pair_gu = KS == 1 && FMT == 4 && p.swiglu_I > 0;
+  const int rowA = pair_gu ? 8 * mt + g : 16 * mt + g;
+  const int rowB = pair_gu ? BOX_ROWS + 8 * mt + g : 16 * mt + g + 8;
   float* ep = reinterpret_cast<float*>(smem + L::EP_OFF);
   float* ep_mine = ep + kh * (TILE_M * L::EP_LD);
   // swizzled word offsets of this thread's K blocks (fmt 4: one chunk a block; fmt 8: two)
@@ -623,17 +678,17 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
     for (int ck = 0; ck < it.nck; ++ck, ++iter) {
       const int s = iter % NSTAGE;
       if (!pipe_wait(&full[s], (iter / NSTAGE) & 1, p.status, abort)) return;
-      const uint8_t* wbox = smem + L::W_OFF + s * W_STAGE_BYTES + (mt >> 1) * (BOX_ROWS * BOX_BYTES);
-      const uint8_t* wr0 = wbox + r0 * BOX_BYTES;
-      const uint8_t* wr1 = wr0 + 8 * BOX_BYTES;
+      const uint8_t* wst = smem + L::W_OFF + s * W_STAGE_BYTES;  // the two boxes, rows 0..63
+      const uint8_t* wr0 = wst + rowA * BOX_BYTES;
+      const uint8_t* wr1 = wst + rowB * BOX_BYTES;
       const uint8_t* sc = smem + L::SC_OFF + s * L::SC_BYTES;
       const uint8_t* act = smem + L::ACT_OFF + s * L::ACT_BYTES + g * ASTR;
       if constexpr (FMT == 4) {
         uint32_t sa[HB / 4], sb[HB / 4];
 #pragma unroll
         for (int j = 0; j < HB / 4; ++j) {
-          sa[j] = lds32(sc + (16 * mt + g) * 8 + 4 * (kh * HB / 4 + j));
-          sb[j] = lds32(sc + (16 * mt + g + 8) * 8 + 4 * (kh * HB / 4 + j));
+          sa[j] = lds32(sc + rowA * 8 + 4 * (kh * HB / 4 + j));
+          sb[j] = lds32(sc + rowB * 8 + 4 * (kh * HB / 4 + j));
         }
         uint32_t wa[HB], wb[HB];
 #pragma unroll
@@ -743,6 +798,9 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
       if (tid == 0) bulk_wait_read();  // this CTA's pushes have read its partial tile
       consumer_bar<NTHR>();
       if (tid < p.ksplit) mbar_arrive_remote(mapa_shared(smem_u32(red_done), tid));  // tile free
+    } else if constexpr (KS == 1 && FMT == 4) {
+      if (*abort) return;
+      epilogue_regs<NT>(p, it, acc, rowA, rowB, c, pair_gu);
     } else {
       const int m0 = 16 * mt + g;
 #pragma unroll
