@@ -114,25 +114,29 @@ int gemm_max_clusters(GemmVariant v, int cluster) {
 
 template <int FMT, int NT, int KS>
 cudaError_t launch_variant(const cudaLaunchConfig_t& cfg, const CUtensorMap& map,
-                           const GemmParams& p) {
-  return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<FMT, NT, Var<FMT, NT, KS>::NSTAGE, KS>, map, p);
+                           const CUtensorMap& smap, const GemmParams& p) {
+  return cudaLaunchKernelEx(&cfg, mx_gemm_kernel<FMT, NT, Var<FMT, NT, KS>::NSTAGE, KS>, map, smap,
+                            p);
 }
 
 cudaError_t launch_gemm(const Launch& L, GemmVariant v, const CUtensorMap& map,
-                        const GemmParams& p, int grid, int cluster) {
+                        const CUtensorMap* smap, const GemmParams& p, int grid, int cluster) {
   int smem = 0, t = 0;
   if (!variant_kernel(v, &smem, &t)) return cudaErrorInvalidValue;
+  if (p.sc_tma && (v.fmt != 4 || !smap)) return cudaErrorInvalidValue;
+  const CUtensorMap& sm = smap ? *smap : map;  // unread unless p.sc_tma
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = config(L, grid, t, smem, cluster, attr);
   if (v.fmt == 8) {
     switch (v.nt) {
-      case 1: return launch_variant<8, 1, 2>(cfg, map, p);
-      case 2: return launch_variant<8, 2, 2>(cfg, map, p);
-      case 4: return launch_variant<8, 4, 2>(cfg, map, p);
-      default: return launch_variant<8, 6, 2>(cfg, map, p);
+      case 1: return launch_variant<8, 1, 2>(cfg, map, sm, p);
+      case 2: return launch_variant<8, 2, 2>(cfg, map, sm, p);
+      case 4: return launch_variant<8, 4, 2>(cfg, map, sm, p);
+      default: return launch_variant<8, 6, 2>(cfg, map, sm, p);
     }
   }
-  return ks_of(v) == 2 ? launch_variant<4, 1, 2>(cfg, map, p) : launch_variant<4, 1, 1>(cfg, map, p);
+  return ks_of(v) == 2 ? launch_variant<4, 1, 2>(cfg, map, sm, p)
+                        : launch_variant<4, 1, 1>(cfg, map, sm, p);
 }
 
 }  // namespace mono

@@ -137,8 +137,9 @@ int gemm_smem_bytes(GemmVariant v);
 cudaError_t gemm_prepare(GemmVariant v);  // raises the dynamic shared-memory limit
 int gemm_ctas_per_sm(GemmVariant v);
 int gemm_max_clusters(GemmVariant v, int cluster);  // co-resident clusters of that size
-// grid must be a multiple of cluster; cluster = p.ksplit for dense matrices, 1 for experts
-cudaError_t launch_gemm(const Launch&, GemmVariant v, const CUtensorMap& map, const GemmParams& p,
-                        int grid, int cluster);
+// grid must be a multiple of cluster; cluster = p.ksplit for dense matrices, 1 for experts.
+// smap: the scale tensor map of an fmt-4 launch with p.sc_tma (else null).
+cudaError_t launch_gemm(const Launch&, GemmVariant v, const CUtensorMap& map,
+                        const CUtensorMap* smap, const GemmParams& p, int grid, int cluster);
 
 }  // namespace mono

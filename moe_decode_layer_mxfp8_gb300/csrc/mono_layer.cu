@@ -61,6 +61,9 @@ struct mono_layer {
   int* perm = nullptr;
   DensePlan dense[D_COUNT];
   CUtensorMap map_ex_gu, map_ex_d;
+  // the expert scale matrices as TMA maps when their rows are whole 16-byte runs
+  CUtensorMap map_ex_gu_s, map_ex_d_s;
+  bool sc_tma_gu = false, sc_tma_d = false;
   int ctas_gemm8[7] = {};  // by nt
   int ex_ctas = 0;      // persistent CTAs of the expert GEMM (large steps)
   int ex_clusters = 0;  // clusters of EXPERT_CLUSTER CTAs of the K-splitting expert GEMM
@@ -102,6 +105,20 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long row_by
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// 2D byte tensor [rows, row_bytes] of E8M0 scales with 16-byte x 32-row boxes, no swizzle;
+// false (and no map) unless the rows are whole 16-byte runs at a 16-byte aligned base.
+bool make_scale_map(CUtensorMap* m, const void* base, long long rows, long long row_bytes) {
+  if (row_bytes % 16 || !aligned16(base)) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {16, BOX_ROWS};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // FFN fields: hidden, the experts, the intermediates, max_rows.  Attention fields only when
 // the handle holds attention weights.
@@ -240,6 +257,9 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
     delete h;
     return MONO_ERR_CUDA;
   }
+  h->sc_tma_gu =
+      make_scale_map(&h->map_ex_gu_s, wt->ex_gu_s, (long long)E * 2 * s.moe_inter, H / 32);
+  h->sc_tma_d = make_scale_map(&h->map_ex_d_s, wt->ex_d_s, (long long)E * H, s.moe_inter / 32);
   const int width = std::max(s.causal ? s.window : s.swa_width, s.window);
   h->attn_min_splits = ffn_only ? 0 : (width + 127) / 128;
   const int attn_splits_max = ffn_only ? 0 : ATTN_MAX_SPLITS;
@@ -443,11 +463,12 @@ cudaError_t dense_launch(const mono_layer* h, int id, int R, const __half* act, 
   p.clamp = h->spec.swiglu_clamp;
   p.status = h->status;
   const int clusters = std::min(d.n_tiles, d.max_clusters[nt]);
-  return launch_gemm(L, {8, nt}, d.map, p, clusters * d.ksplit, d.ksplit);
+  return launch_gemm(L, {8, nt}, d.map, nullptr, p, clusters * d.ksplit, d.ksplit);
 }
 
 // One MXFP4 routed-expert GEMM over the R * topk (row, slot) pairs grouped by expert.
-cudaError_t expert_launch(const mono_layer* h, int R, const CUtensorMap& map, const uint8_t* sc,
+cudaError_t expert_launch(const mono_layer* h, int R, const CUtensorMap& map,
+                          const CUtensorMap* smap, const uint8_t* sc,
                           int Kdim, int rows_per_mat, int swiglu, int n_tiles, const __half* act,
                           int act_ld, const int* rowmap, int epi, void* outp, int out_ld,
                           const Launch& L) {
@@ -473,9 +494,11 @@ cudaError_t expert_launch(const mono_layer* h, int R, const CUtensorMap& map, co
   p.out_ld = out_ld;
   p.clamp = h->spec.swiglu_clamp;
   p.status = h->status;
+  p.sc_tma = smap != nullptr;
   if (small)
-    return launch_gemm(L, {4, 1, 2}, map, p, h->ex_clusters * EXPERT_CLUSTER, EXPERT_CLUSTER);
-  return launch_gemm(L, {4, 1, 1}, map, p, h->ex_ctas, 1);
+    return launch_gemm(L, {4, 1, 2}, map, smap, p, h->ex_clusters * EXPERT_CLUSTER,
+                       EXPERT_CLUSTER);
+  return launch_gemm(L, {4, 1, 1}, map, smap, p, h->ex_ctas, 1);
 }
 
 // Inputs of the FFN half of a step (shared by the whole-layer step and the FFN launch).
@@ -544,12 +567,14 @@ int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
   const bool late_join = fork && R * K > EXPERT_SMALL_SLOTS;
   if (fork && !late_join) TRY_CUDA(cudaStreamWaitEvent(stream, h->ev_join, 0));
   TRY(run([&] {
-    return expert_launch(h, R, h->map_ex_gu, h->w.ex_gu_s, H, 2 * s.moe_inter, s.moe_inter,
+    return expert_launch(h, R, h->map_ex_gu, h->sc_tma_gu ? &h->map_ex_gu_s : nullptr,
+                         h->w.ex_gu_s, H, 2 * s.moe_inter, s.moe_inter,
                          s.moe_inter / BOX_ROWS, h->buf<__half>(MONO_BUF_U), H, h->perm,
                          EPI_SWIGLU_F16, h->buf<void>(MONO_BUF_TR), s.moe_inter, L);
   }));
   TRY(run([&] {
-    return expert_launch(h, R, h->map_ex_d, h->w.ex_d_s, s.moe_inter, H, 0, H / TILE_M,
+    return expert_launch(h, R, h->map_ex_d, h->sc_tma_d ? &h->map_ex_d_s : nullptr,
+                         h->w.ex_d_s, s.moe_inter, H, 0, H / TILE_M,
                          h->buf<__half>(MONO_BUF_TR), s.moe_inter, nullptr, EPI_F32,
                          h->buf<void>(MONO_BUF_YR), H, L);
   }));

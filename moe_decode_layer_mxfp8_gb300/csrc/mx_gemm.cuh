@@ -82,6 +82,7 @@ struct GemmParams {
   int dense_rows;         // dense mode: activation rows
   int n_tiles;            // work tiles per matrix
   int ksplit;             // dense mode: K splits per tile = cluster size
+  int sc_tma;             // fmt 4: scales by TMA (16-byte x 32-row boxes of the scale tensor map)
   const RouteInfo* route; // non-null selects expert mode
   int epi;
   void* out;
@@ -104,7 +105,10 @@ template <>
 struct FmtTraits<4> {
   static constexpr int KC = 256;
   static constexpr int ACT_STRIDE = 256 * 2 + 64;
-  static constexpr int SC_BYTES = TILE_M * 8;  // 64 weight rows x 8 K blocks
+  // 64 weight rows x 16 bytes: the 16-byte aligned run of scale bytes that holds the
+  // stage's 8 K blocks (at byte (k0 / 32) & 8 of the run)
+  static constexpr int SC_ROW = 16;
+  static constexpr int SC_BYTES = TILE_M * SC_ROW;
 };
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -248,6 +252,7 @@ __device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity, int* s
 // cp.async arrival per lane issued after the activation copies.
 template <int FMT, int NT, int NSTAGE, int KS>
 __device__ __forceinline__ void issue_weights(const GemmParams& p, const CUtensorMap* map,
+                                              const CUtensorMap* smap,
                                               uint8_t* smem, uint64_t* full, const Item& it,
                                               int c, int s, int lane) {
   using L = GemmLayout<FMT, NT, NSTAGE, KS>;
@@ -264,24 +269,35 @@ __device__ __forceinline__ void issue_weights(const GemmParams& p, const CUtenso
       cp_async4(sst + lane * 4, ok ? (const void*)src : (const void*)p.scales,
                 ok ? (uint32_t)min(4, nkb) : 0u);
     }
-  } else {
+  } else if (!p.sc_tma) {
+    // scale rows that are not whole 16-byte runs: two 4-byte copies per weight row, placed
+    // where the TMA path puts them
+    constexpr int SC_ROW = FmtTraits<4>::SC_ROW;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const bool ok = half == 0 ? it.a_ok : it.b_ok;
       const long long row = (long long)(half == 0 ? it.sc_a : it.sc_b) + lane;
       const uint8_t* src = p.scales + row * p.scale_ld + kb0;
-      uint8_t* dst = sst + (half * BOX_ROWS + lane) * 8;
+      uint8_t* dst = sst + (half * BOX_ROWS + lane) * SC_ROW + (kb0 & 8);
       const int n0 = ok ? min(4, nkb) : 0, n1 = ok ? max(0, min(4, nkb - 4)) : 0;
       cp_async4(dst, n0 ? (const void*)src : (const void*)p.scales, (uint32_t)n0);
       cp_async4(dst + 4, n1 ? (const void*)(src + 4) : (const void*)p.scales, (uint32_t)n1);
     }
   }
   if (lane == 0) {
-    mbar_arrive_expect_tx(&full[s], W_STAGE_BYTES);
+    // fmt 4 with sc_tma: the two boxes' scale runs (16 bytes x 32 rows each) by TMA too, in
+    // place of 64 four-byte copies a stage
+    constexpr uint32_t SC_BOX = FmtTraits<4>::SC_ROW * BOX_ROWS;
+    const bool sc_tma = FMT == 4 && p.sc_tma;
+    mbar_arrive_expect_tx(&full[s], W_STAGE_BYTES + (sc_tma ? 2 * SC_BOX : 0u));
     const int xb = FMT == 8 ? k0 : k0 / 2;
     uint8_t* wst = smem + L::W_OFF + s * W_STAGE_BYTES;
     tma_load_2d(wst, map, xb, it.wrow_a, &full[s]);
     tma_load_2d(wst + BOX_ROWS * BOX_BYTES, map, xb, it.wrow_b, &full[s]);
+    if (sc_tma) {
+      tma_load_2d(sst, smap, kb0 & ~15, it.sc_a, &full[s]);
+      tma_load_2d(sst + SC_BOX, smap, kb0 & ~15, it.sc_b, &full[s]);
+    }
   }
 }
 
@@ -333,14 +349,15 @@ __device__ int prefetch_weights(const GemmParams& p, const CUtensorMap* map, uin
   Item it;
   decode_item<FMT>(p, nullptr, blockIdx.x, ks, it);
   const int pre = min(NSTAGE, it.nck);
-  for (int c = 0; c < pre; ++c) issue_weights<FMT, NT, NSTAGE, KS>(p, map, smem, full, it, c, c, lane);
+  for (int c = 0; c < pre; ++c)
+    issue_weights<FMT, NT, NSTAGE, KS>(p, map, map, smem, full, it, c, c, lane);
   return pre;
 }
 
 template <int FMT, int NT, int NSTAGE, int KS>
 __device__ void gemm_producer(const GemmParams& p, const RouteSmem* rs, const CUtensorMap* map,
-                              uint8_t* smem, uint64_t* full, uint64_t* empty,
-                              volatile int* abort, int pre) {
+                              const CUtensorMap* smap, uint8_t* smem, uint64_t* full,
+                              uint64_t* empty, volatile int* abort, int pre) {
   const int lane = threadIdx.x & 31;
   const int ks = split_of(p, rs);
   const int n_items = total_items(p, rs, ks);
@@ -352,7 +369,7 @@ __device__ void gemm_producer(const GemmParams& p, const RouteSmem* rs, const CU
       const int s = iter % NSTAGE;
       const uint32_t ph = (iter / NSTAGE) & 1;
       if (!pipe_wait(&empty[s], ph ^ 1, p.status, abort)) goto drain;
-      if (iter >= pre) issue_weights<FMT, NT, NSTAGE, KS>(p, map, smem, full, it, c, s, lane);
+      if (iter >= pre) issue_weights<FMT, NT, NSTAGE, KS>(p, map, smap, smem, full, it, c, s, lane);
       issue_acts<FMT, NT, NSTAGE, KS>(p, rs, smem, full, it, c, s, lane);
     }
   }
@@ -684,11 +701,14 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
       const uint8_t* sc = smem + L::SC_OFF + s * L::SC_BYTES;
       const uint8_t* act = smem + L::ACT_OFF + s * L::ACT_BYTES + g * ASTR;
       if constexpr (FMT == 4) {
+        // this stage's 8 scale bytes of a row sit at byte (k0 / 32) & 8 of its 16-byte run
+        constexpr int SC_ROW = FmtTraits<4>::SC_ROW;
+        const int soff = ((it.k0 + ck * FmtTraits<4>::KC) / 32) & 8;
         uint32_t sa[HB / 4], sb[HB / 4];
 #pragma unroll
         for (int j = 0; j < HB / 4; ++j) {
-          sa[j] = lds32(sc + rowA * 8 + 4 * (kh * HB / 4 + j));
-          sb[j] = lds32(sc + rowB * 8 + 4 * (kh * HB / 4 + j));
+          sa[j] = lds32(sc + rowA * SC_ROW + soff + 4 * (kh * HB / 4 + j));
+          sb[j] = lds32(sc + rowB * SC_ROW + soff + 4 * (kh * HB / 4 + j));
         }
         uint32_t wa[HB], wb[HB];
 #pragma unroll
@@ -837,7 +857,8 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
 
 template <int FMT, int NT, int NSTAGE, int KS>
 __global__ void __launch_bounds__(gemm_threads(KS), FMT == 4 && KS == 1 ? 4 : 2)
-    mx_gemm_kernel(const __grid_constant__ CUtensorMap map, const GemmParams p) {
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap map,
+                   const __grid_constant__ CUtensorMap smap, const GemmParams p) {
   using L = GemmLayout<FMT, NT, NSTAGE, KS>;
   constexpr int CONSUMER_WARPS = 4 * KS, THREADS = gemm_threads(KS);
   extern __shared__ uint8_t smem_raw[];
@@ -860,7 +881,10 @@ __global__ void __launch_bounds__(gemm_threads(KS), FMT == 4 && KS == 1 ? 4 : 2)
     fence_mbar_init();
     *abort = 0;
   }
-  if (warp == CONSUMER_WARPS && (threadIdx.x & 31) == 0) prefetch_tmap(&map);
+  if (warp == CONSUMER_WARPS && (threadIdx.x & 31) == 0) {
+    prefetch_tmap(&map);
+    if (FMT == 4 && p.sc_tma) prefetch_tmap(&smap);
+  }
   // every CTA of a cluster must have initialised its barriers before any remote arrival
   if (clustered)
     cluster_sync_all();
@@ -897,7 +921,7 @@ __global__ void __launch_bounds__(gemm_threads(KS), FMT == 4 && KS == 1 ? 4 : 2)
     }
   }
   if (warp == CONSUMER_WARPS)
-    gemm_producer<FMT, NT, NSTAGE, KS>(p, rs, &map, smem, full, empty, abort, pre);
+    gemm_producer<FMT, NT, NSTAGE, KS>(p, rs, &map, &smap, smem, full, empty, abort, pre);
   else
     gemm_consumer<FMT, NT, NSTAGE, KS>(p, rs, smem, full, empty, red_full, red_done, abort);
 }
