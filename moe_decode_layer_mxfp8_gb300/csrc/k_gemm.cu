@@ -124,6 +124,9 @@ cudaError_t launch_gemm(const Launch& L, GemmVariant v, const CUtensorMap& map,
   int smem = 0, t = 0;
   if (!variant_kernel(v, &smem, &t)) return cudaErrorInvalidValue;
   if (p.sc_tma && (v.fmt != 4 || !smap)) return cudaErrorInvalidValue;
+  // the large-step routed-expert variant: no cluster, and a work counter
+  if (v.fmt == 4 && ks_of(v) == 1 && (cluster != 1 || p.ksplit != 1 || !p.item_next))
+    return cudaErrorInvalidValue;
   const CUtensorMap& sm = smap ? *smap : map;  // unread unless p.sc_tma
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = config(L, grid, t, smem, cluster, attr);

@@ -175,6 +175,9 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
     if (dry.e == -2) s_pos[0] = 0;  // never true: keeps the call
   }
   pdl_wait();
+  // the routed-expert GEMMs of this step take their work items from these counters; every
+  // earlier kernel of the stream has completed once this CTA is past its wait
+  if (tid == 0) a.route->item_next[0] = a.route->item_next[1] = 0;
   // phase 1a: logits = the K-slice partials summed in slice order
   const int nz = a.rows * a.E;
   for (int base = tid; base < nz; base += TOPK_BATCH * TOPK_THREADS) {

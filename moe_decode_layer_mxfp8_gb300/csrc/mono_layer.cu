@@ -495,6 +495,8 @@ cudaError_t expert_launch(const mono_layer* h, int R, const CUtensorMap& map,
   p.clamp = h->spec.swiglu_clamp;
   p.status = h->status;
   p.sc_tma = smap != nullptr;
+  // large steps schedule items dynamically over the counter the top-k zeroes each step
+  p.item_next = small ? nullptr : h->route->item_next + (swiglu > 0 ? 0 : 1);
   if (small)
     return launch_gemm(L, {4, 1, 2}, map, smap, p, h->ex_clusters * EXPERT_CLUSTER,
                        EXPERT_CLUSTER);

@@ -50,6 +50,7 @@ struct RouteInfo {
   int hit_off[MAX_EXPERTS];        // first expert-sorted position of its rows
   int hit_cnt[MAX_EXPERTS];        // number of rows routed to it
   int rg_prefix[MAX_EXPERTS + 1];  // prefix sum of ceil(hit_cnt / EXPERT_ROWS)
+  int item_next[2];                // work counters of the large-step gate_up / down launches
 };
 
 // Shared-memory copy of the routing metadata plus the activation row map, and the hit
@@ -83,6 +84,7 @@ struct GemmParams {
   int n_tiles;            // work tiles per matrix
   int ksplit;             // dense mode: K splits per tile = cluster size
   int sc_tma;             // fmt 4: scales by TMA (16-byte x 32-row boxes of the scale tensor map)
+  int* item_next;         // large-step routed experts: the launch's work counter, zero at entry
   const RouteInfo* route; // non-null selects expert mode
   int epi;
   void* out;
@@ -132,7 +134,9 @@ struct GemmLayout {
   static constexpr int BAR_OFF = align_up(ROUTE_OFF + ROUTE_BYTES, 16);
   // full[NSTAGE], empty[NSTAGE], red_full, red_done
   static constexpr int MISC_OFF = BAR_OFF + (2 * NSTAGE + 2) * 8;
-  static constexpr int BYTES = MISC_OFF + 16 + 1024;  // + slack for 1024-byte alignment
+  // per ring slot: the work item whose first stage it holds (dynamically scheduled launches)
+  static constexpr int SLOTQ_OFF = MISC_OFF + 16;
+  static constexpr int BYTES = SLOTQ_OFF + align_up(4 * NSTAGE, 16) + 1024;  // + alignment slack
 };
 
 struct Item {
@@ -244,6 +248,11 @@ __device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity, int* s
     }
   }
 }
+
+// The large-step routed-expert kernel (one K share, never a cluster) schedules its work items
+// dynamically; every other variant takes a fixed share.
+template <int FMT, int KS>
+constexpr bool DYNAMIC_ITEMS = FMT == 4 && KS == 1;
 
 // ------------------------------------------------------------------------------ producer
 // A stage has two independent halves: the weight tile with its scales (constant data, safe
@@ -358,20 +367,50 @@ template <int FMT, int NT, int NSTAGE, int KS>
 __device__ void gemm_producer(const GemmParams& p, const RouteSmem* rs, const CUtensorMap* map,
                               const CUtensorMap* smap, uint8_t* smem, uint64_t* full,
                               uint64_t* empty, volatile int* abort, int pre) {
+  using L = GemmLayout<FMT, NT, NSTAGE, KS>;
   const int lane = threadIdx.x & 31;
   const int ks = split_of(p, rs);
   const int n_items = total_items(p, rs, ks);
+  volatile int* slot_q = reinterpret_cast<volatile int*>(smem + L::SLOTQ_OFF);
   int iter = 0;
-  for (int q = blockIdx.x; q < n_items; q += gridDim.x) {
+  // Large-step routed experts take their items from the launch's counter (a CTA that becomes
+  // resident late, behind another stream's kernel, then finds little or no work left instead
+  // of a fixed share), fetching the next index while the current item streams; the others
+  // take every gridDim.x-th item.
+  int q = blockIdx.x, qn = 0;
+  if constexpr (DYNAMIC_ITEMS<FMT, KS>) {
+    if (lane == 0) q = atomicAdd(p.item_next, 1);
+    q = __shfl_sync(0xffffffffu, q, 0);
+  }
+  while (q < n_items) {
+    if constexpr (DYNAMIC_ITEMS<FMT, KS>) {
+      if (lane == 0) qn = atomicAdd(p.item_next, 1);
+    }
     Item it;
     decode_item<FMT>(p, rs, q, ks, it);
     for (int c = 0; c < it.nck; ++c, ++iter) {
       const int s = iter % NSTAGE;
       const uint32_t ph = (iter / NSTAGE) & 1;
       if (!pipe_wait(&empty[s], ph ^ 1, p.status, abort)) goto drain;
+      // published before lane 0's arrival on the stage's barrier (a release) in issue_weights
+      if (DYNAMIC_ITEMS<FMT, KS> && c == 0 && lane == 0) slot_q[s] = q;
       if (iter >= pre) issue_weights<FMT, NT, NSTAGE, KS>(p, map, smap, smem, full, it, c, s, lane);
       issue_acts<FMT, NT, NSTAGE, KS>(p, rs, smem, full, it, c, s, lane);
     }
+    if constexpr (DYNAMIC_ITEMS<FMT, KS>)
+      q = __shfl_sync(0xffffffffu, qn, 0);
+    else
+      q += gridDim.x;
+  }
+  if constexpr (DYNAMIC_ITEMS<FMT, KS>) {
+    // the end: one more stage that carries no data, only the end mark
+    const int s = iter % NSTAGE;
+    if (!pipe_wait(&empty[s], ((iter / NSTAGE) & 1) ^ 1, p.status, abort)) goto drain;
+    if (lane == 0) {
+      slot_q[s] = -1;
+      mbar_arrive(&full[s]);
+    }
+    cp_async_arrive_noinc(&full[s]);  // the other 32 arrivals of the phase
   }
   return;
 drain:
@@ -684,7 +723,18 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
   const bool clustered = ks > 1;
   const uint32_t rank = clustered ? cluster_ctarank() : 0u;
   int iter = 0, tiles_done = 0;
-  for (int q = blockIdx.x; q < n_items; q += gridDim.x) {
+  const volatile int* slot_q = reinterpret_cast<const volatile int*>(smem + L::SLOTQ_OFF);
+  for (int q = blockIdx.x;; q += gridDim.x) {
+    if constexpr (DYNAMIC_ITEMS<FMT, KS>) {
+      // the next stage holds the next item's first K chunk and its index, or the end mark
+      // (the stage loop below waits on it again, which then returns at once)
+      const int s = iter % NSTAGE;
+      if (!pipe_wait(&full[s], (iter / NSTAGE) & 1, p.status, abort)) return;
+      q = slot_q[s];
+      if (q < 0) break;
+    } else if (q >= n_items) {
+      break;
+    }
     Item it;
     decode_item<FMT>(p, rs, q, ks, it);
     const int ntl = (it.n + 7) >> 3;
