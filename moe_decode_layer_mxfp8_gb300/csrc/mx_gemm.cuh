@@ -13,16 +13,21 @@
 // one item per (expert, 64 rows, up to 8 routed rows) and the full K; the routing metadata
 // is staged in shared memory once per CTA.
 //
-// CTA = 1 producer warp + 8 consumer warps, persistent over items.  The producer streams
-// weight tiles with cp.async.bulk.tensor (128-byte swizzle) and the activation / scale
-// chunks with cp.async into an NSTAGE ring guarded by mbarriers; for dense matrices it
-// issues the first stages' weights before waiting on the previous kernel, so that weight
-// streaming overlaps it.  Consumer warp w owns tile rows 16w..16w+15: it decodes its weight
-// fragment in registers (cvt e2m1x2 / e4m3x2 -> f16x2), runs m16n8k16 MMAs per 32-wide K
-// block against every 8-row activation tile, and applies the block's E8M0 scale to the
-// block's f32 result.  Within a 32-wide block the
-// MMA's 16 K slots are a fixed permutation of the block's K positions, applied to both
-// operands, which leaves the dot product unchanged.
+// CTA = 1 producer warp + 4*KS consumer warps (4 M-tiles x KS K-shares), persistent over
+// items: a fixed share per CTA, except in the large-step routed-expert kernel, whose producer
+// takes items from a per-launch counter and passes each one to the consumers in the ring
+// slot of its first stage.  The producer streams weight tiles with cp.async.bulk.tensor
+// (128-byte swizzle), the routed experts' E8M0 scales as 16-byte x 32-row TMA boxes, and
+// the activation rows (bulk copies, or 16-byte cp.async for dense matrices) into an NSTAGE
+// ring guarded by mbarriers; for dense matrices it issues the first stages' weights before
+// waiting on the previous kernel, so that weight streaming overlaps it.  A consumer warp
+// owns 16 tile rows (16mt..16mt+15, or in the large-step SwiGLU tiles 8 gate rows with
+// their up rows): it decodes its weight fragment in registers (cvt e2m1x2 / e4m3x2 ->
+// f16x2), runs m16n8k16 MMAs per 32-wide K block against every 8-row activation tile, and
+// applies the block's E8M0 scale to the block's f32 result (or, for MXFP8 with many
+// activation tiles, to the decoded weights while that is exact in f16).  Within a 32-wide
+// block the MMA's 16 K slots are a fixed permutation of the block's K positions, applied to
+// both operands, which leaves the dot product unchanged.
 #pragma once
 
 #include "common.cuh"
