@@ -212,15 +212,13 @@ def measure_device(name, steps, warmup, dev, n_copies, sampler=None):
             byte_list.append(step_bytes(spec, step, idx.cpu().numpy()))
         for lay, _ in layers:
             assert lay.status() == 0
-        big_n = C * max(1, 64 // C)
-        big = _capture(layers, step, outs, stream, big_n)
+        # one graph per layer copy holding one step, replayed once per step (a graph of 64
+        # consecutive steps measured ~4 us a step slower at 48 rows)
         ones = [_capture([layers[c]], step, [outs[c]], stream, 1) for c in range(C)]
     torch.cuda.synchronize(dev)
 
     def run(k):
-        for _ in range(k // big_n):
-            big.replay()
-        for i in range(k % big_n):
+        for i in range(k):
             ones[i % C].replay()
 
     with torch.cuda.stream(stream):
@@ -317,7 +315,8 @@ def ffn_bytes(spec: dict, rows: int, d_hit: int) -> int:
 def measure_ffn(rows, steps, warmup, dev, n_copies):
     """The FFN launch (residual from an attention output, then the FFN seam and the MoE) on
     the first `rows` rows of the 48-row step (6 rows = one request of 6 tokens), on FFN-only
-    handles rotating over n_copies distinct weight sets, replayed from one CUDA graph."""
+    handles rotating over n_copies distinct weight sets, each launch replayed from its copy's
+    one-launch CUDA graph."""
     import moe_decode_layer_mxfp8_gb300 as m
     name = "full_r48"
     wl = gen.WORKLOADS[name]
@@ -342,27 +341,29 @@ def measure_ffn(rows, steps, warmup, dev, n_copies):
             stream.synchronize()
             d_hit.append(len(np.unique(idx.cpu().numpy())))
             assert lay.status() == 0
-        n_graph = len(layers) * max(1, 64 // len(layers))
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(n_graph):
-                layers[i % len(layers)].ffn_step(x, a, outs[i % len(layers)], pos, stream=stream)
-        for _ in range(max(3, warmup)):
-            g.replay()
+        # one graph per weight copy holding one launch, replayed once per launch
+        gs = []
+        for c, lay in enumerate(layers):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                lay.ffn_step(x, a, outs[c], pos, stream=stream)
+            gs.append(g)
+        for i in range(max(3, warmup)):
+            gs[i % len(gs)].replay()
     torch.cuda.synchronize(dev)
-    reps = max(1, steps // n_graph)
+    n = max(len(gs), steps)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         t0.record(stream)
-        for _ in range(reps):
-            g.replay()
+        for i in range(n):
+            gs[i % len(gs)].replay()
         t1.record(stream)
     torch.cuda.synchronize(dev)
-    us = t0.elapsed_time(t1) * 1000.0 / (reps * n_graph)
+    us = t0.elapsed_time(t1) * 1000.0 / n
     byts = float(np.mean([ffn_bytes(spec, rows, d) for d in d_hit]))
     for lay in layers:
         lay.close()
-    del layers, g
+    del layers, gs
     torch.cuda.empty_cache()
     return dict(rows=rows, us_per_launch=round(us, 2), hbm_gbs=round(byts / us / 1e3, 1),
                 bytes_per_launch=int(byts), d_hit=d_hit, copies=n_copies)
@@ -401,7 +402,8 @@ def measure_e2e(res, steps, warmup, dev):
     and its output copied back out, all inside the timed region.  The copies run on a copy
     stream with two sets of device buffers, so that step i + 1's inputs arrive and step
     i - 1's output leaves while step i computes (each step's copies still bracket its own
-    compute)."""
+    compute).  The step itself is the public call captured once per (layer copy, buffer
+    set) into a CUDA graph and replayed, as a serving loop would run it."""
     spec, step, layers = res["spec"], res["step"], res["layers"]
     stream = res["stream"]
     copy = torch.cuda.Stream(dev)
@@ -424,16 +426,35 @@ def measure_e2e(res, steps, warmup, dev):
                 d_in[b][k].copy_(t, non_blocking=True)
             ev_in[b].record(copy)
 
+    graphs = {}
+
+    def step_graph(li, b):
+        if (li, b) not in graphs:
+            lay, _ = layers[li]
+            d = d_in[b]
+            with torch.cuda.stream(stream):  # one eager call first, then the capture
+                lay.step(d["x"], d_out[b], d["positions"], d["row_req"], d["block_table"],
+                         step["kv_cache"], stream=stream)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                lay.step(d["x"], d_out[b], d["positions"], d["row_req"], d["block_table"],
+                         step["kv_cache"], stream=stream)
+            graphs[(li, b)] = g
+        return graphs[(li, b)]
+
+    for i in range(2 * len(layers)):  # every (layer copy, buffer set) the loop uses
+        step_graph(i % len(layers), i % 2)
+    torch.cuda.synchronize(dev)
+
     def compute(i):
         b = i % 2
-        lay, _ = layers[i % len(layers)]
+        g = step_graph(i % len(layers), b)
         with torch.cuda.stream(stream):
             stream.wait_event(ev_in[b])
             if used[b]:  # step i - 2's output has left this buffer
                 stream.wait_event(ev_out[b])
-            d = d_in[b]
-            lay.step(d["x"], d_out[b], d["positions"], d["row_req"], d["block_table"],
-                     step["kv_cache"], stream=stream)
+            g.replay()
             ev_done[b].record(stream)
         used[b] = True
 
@@ -692,7 +713,8 @@ def main():
                     layer_copies=res["copies"],
                     l2=f"inputs larger than L2: weights rotate over {res['copies']} distinct layer "
                        f"copies ({res['bytes'] / 1e6:.0f} MB touched per step, L2 {l2 / 1e6:.0f} MB)",
-                    graph="CUDA graphs of programmatically serialised launches"),
+                    graph="each step replayed from a one-step CUDA graph of programmatically "
+                          "serialised launches"),
         hbm_gbs=round(gbs, 1), frac_of_8tbs=round(gbs / NOMINAL_HBM_GBS, 4),
         frac_of_measured_copy=round(gbs / peak, 4), bytes_per_step=int(res["bytes"]),
         d_hit=res["d_hit"],
