@@ -198,3 +198,48 @@ def test_router_force_idx(orc):
     p = res["probs"]
     for r in range(2):
         np.testing.assert_allclose(res["w"][r], p[r, forced[r]] / p[r, forced[r]].sum())
+
+
+# ------------------------------------------------------------------ attention scale pin
+def test_attention_score_scale_two_key_closed_form(orc):
+    """Scaled dot-product attention (softmax(q . k / sqrt(head_dim))) pinned by a closed form.
+
+    One row at position 1 with a causal window of 2 sees two keys.  In latent slice g the
+    newer key holds 2 at element 0 and (1 + g/4) at element 1, the older key 0 and -1; head
+    h's query is a_h e_0.  The score difference is then 2 a_h / sqrt(64), so the newer key's
+    weight is w = 1 / (1 + exp(-2 a_h / 8)) and o_h[0] = 2 w, o_h[1] = (1 + g/4) w - (1 - w).
+    Scales 1/sqrt(kv_dim) = 1/16, 1/head_dim and 1 give weights off by far more than a bf16
+    rounding, and a wrong head -> slice map changes o_h[1]; both would fail."""
+    nq, dh, kvd = 4, 64, 256                       # 4 latent slices, one head each
+    rec_bytes = 272
+    spec = dict(gen.spec_of("tiny"), n_q_heads=nq, head_dim=dh, kv_dim=kvd, window=2,
+                swa_width=2, causal=1, block_size=16, kv_record_bytes=rec_bytes)
+    cache = np.zeros((1, 16, rec_bytes), np.uint8)
+    one = np.frombuffer(np.float32(1.0).tobytes(), np.uint8)
+    e4m3 = {2.0: 0x40, 1.0: 0x38, 1.25: 0x3A, 1.5: 0x3C, 1.75: 0x3E, -1.0: 0xB8}
+    for g in range(nq):
+        cache[0, 1, g * dh + 0] = e4m3[2.0]
+        cache[0, 1, g * dh + 1] = e4m3[1.0 + g / 4]
+        cache[0, 0, g * dh + 1] = e4m3[-1.0]
+    cache[0, 0, kvd:kvd + 4] = one
+    cache[0, 1, kvd:kvd + 4] = one
+    a = np.array([4.375, 1.5, -2.0, 0.75])         # exact in bf16
+    q = np.zeros(nq * dh)
+    q[np.arange(nq) * dh] = a
+    st = dict(x=np.zeros((1, spec["hidden"]), np.uint16), positions=np.array([1], np.int32),
+              row_req=np.array([0], np.int32), block_table=np.zeros((1, 1), np.int32),
+              kv_cache=cache)
+    rc, o = orc.attention(spec, st, _bf16(q[None, :]))
+    assert rc == 0
+    got = bf16_f64(o[0]).reshape(nq, dh)
+
+    def expect(scale):
+        w = 1.0 / (1.0 + np.exp(-2.0 * a * scale))
+        g = np.arange(nq)
+        return np.stack([2 * w, (1 + g / 4) * w - (1 - w)], axis=1)
+
+    want = expect(1.0 / np.sqrt(dh))
+    np.testing.assert_allclose(got[:, :2], want, rtol=2.0 ** -8, atol=0)
+    assert not got[:, 2:].any()                    # every other element is zero in both keys
+    for wrong in (1.0 / np.sqrt(kvd), 1.0 / dh, 1.0):
+        assert np.abs(expect(wrong) - want).max() > 8 * 2.0 ** -8 * np.abs(want).max()
