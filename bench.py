@@ -237,10 +237,25 @@ def measure_device(name, steps, warmup, dev, n_copies, sampler=None):
     if torch.distributed.is_initialized():
         torch.distributed.barrier()
     us = ms * 1000.0 / steps
+    # the distribution of single steps: an event before and after each of >= 100 replays
+    n_rep = max(100, min(steps, 500))
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(n_rep):
+            ones[i % C].replay()
+            evs[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    per = np.array([evs[i].elapsed_time(evs[i + 1]) * 1000.0 for i in range(n_rep)])
+    dist = dict(replays=n_rep, median=round(float(np.median(per)), 2),
+                p10=round(float(np.percentile(per, 10)), 2),
+                p90=round(float(np.percentile(per, 90)), 2),
+                mean=round(float(per.mean()), 2))
     # bytes per step averaged over the rotation actually run
     seq = [byte_list[i % C]["total"] for i in range(steps)]
     avg_bytes = float(np.mean(seq))
     res = dict(spec=spec, step=step, layers=layers, outs=outs, stream=stream, us=us, ms=ms,
+               dist=dist,
                bytes=avg_bytes, bytes_detail=byte_list[0], d_hit=[b["d_hit"] for b in byte_list],
                launches=steps * layers[0][0].launches_per_step(), copies=C)
     return res
@@ -486,22 +501,77 @@ def measure_e2e(res, steps, warmup, dev):
     return dict(value=us, unit=UNIT, h2d_bytes_per_step=int(h2d_b), d2h_bytes_per_step=int(d2h_b))
 
 
-def cpu_baseline(res):
-    """The oracle, as it stands, on the host cores: one full layer step of the headline
-    workload (all rows) on every core."""
+def _cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+CPU_WORKLOADS = ("full_r1", "draft_r6", "full_r48")
+
+
+def cpu_baseline(dev):
+    """The oracle, as it stands, on the host cores (a reported baseline, not a target): one
+    full layer step of each single-layer configuration (1 row, 6 draft rows, 48 rows), once
+    single-threaded and once with OpenMP over every core, and the stacked 30-layer step
+    extrapolated from two distinct 48-row layers on every core (x 15).  The value is the
+    headline 48-row step on every core.  About 25 s of host time."""
     import oracle
-    from tests.helpers import to_np
-    spec, step = res["spec"], res["step"]
-    w = {k: to_np(v) for k, v in res["layers"][0][1].items()}
-    s = {k: (to_np(v) if isinstance(v, torch.Tensor) else v) for k, v in step.items()}
+    from tests.helpers import np_inputs
+    oracle.build()
     cores = os.cpu_count() or 1
+    per = {}
+    keep = None
+    for name in CPU_WORKLOADS:
+        spec, wl = gen.spec_of(name), gen.WORKLOADS[name]
+        w = gen.make_weights(spec, wl["seed"], device=dev)
+        wn, sn = np_inputs(w, gen.make_step(spec, wl))
+        del w
+        d = {}
+        for threads in (1, cores):
+            oracle.set_threads(threads)
+            t = time.perf_counter()
+            out = oracle.layer(spec, wn, sn)["out"]
+            d["us_1_thread" if threads == 1 else "us_all_cores"] = round(
+                (time.perf_counter() - t) * 1e6, 1)
+        per[name] = d
+        if name == HEADLINE:
+            keep = (spec, wn, sn, out)
+    # the stacked step: a second 48-row layer with its own weights on the first one's output
+    spec, wn, sn, out = keep
+    w2 = gen.make_weights(spec, gen.WORKLOADS[HEADLINE]["seed"] + 1000, device=dev)
+    wn2, _ = np_inputs(w2, {})
+    del w2
     oracle.set_threads(cores)
     t = time.perf_counter()
-    oracle.layer(spec, w, s)
-    dt = time.perf_counter() - t
-    return dict(value=dt * 1e6, unit=UNIT, cores=cores, kind="oracle",
-                sample=f"one full {res['step']['rows']}-row layer step of the headline workload "
-                       f"(weights copy 0), OpenMP over {cores} host threads")
+    out1 = oracle.layer(spec, wn, sn)["out"]
+    oracle.layer(spec, wn2, dict(sn, x=out1))
+    two = time.perf_counter() - t
+    v = per[HEADLINE]["us_all_cores"]
+    return dict(value=v, unit=UNIT, cores=cores, kind="oracle", cpu_model=_cpu_model(),
+                nproc=cores,
+                sample=f"one full {sn['x'].shape[0]}-row layer step of the headline workload, "
+                       f"OpenMP over {cores} host threads; per_workload: one step of each "
+                       f"configuration single-threaded and on every core",
+                per_workload=per,
+                stacked_30x48_extrapolated=dict(
+                    us=round(two * 15 * 1e6, 1),
+                    note="two distinct 48-row layers timed on every core (the second on the "
+                         "first's output), times 15: an extrapolation, not a measurement"))
 
 
 # ------------------------------------------------------------------------ reference arm
@@ -564,8 +634,8 @@ def _workload_desc(name, spec, rows):
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the dominant
-# kernel, from the ncu capture summarised in profiles/expert_gate_up_full_r48.md, keyed by
-# the md5 of the GEMM sources it was taken on: reported only while those are unchanged.
+# kernel, from an ncu capture of one launch, keyed by the md5 of the GEMM sources it was
+# taken on: reported only while those are unchanged.
 NCU_TRAFFIC = {
     ("full_r48", "expert_gate_up"): (499_593_216, "6fe50f48436f2a0ffda5000e987420f8"
                                                   "11ea0d6a1dd3a6dc5a7280a56fec6f62"
@@ -611,8 +681,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--workload", default=HEADLINE, choices=["full_r48", "full_r1", "draft_r6"])
     ap.add_argument("--eager", type=int, default=0, metavar="N",
-                    help="only run N eager steps of the workload (one layer copy) and exit: the "
-                         "command the ncu captures under profiles/ run")
+                    help="only run N eager steps of the workload (one layer copy) and exit: a "
+                         "short command for ncu captures of single launches")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.eager:
@@ -661,6 +731,7 @@ def main():
                     continue
                 r = measure_device(name, min(args.steps, 2000), args.warmup, dev, copies_for(name))
                 sweep[name] = dict(rows=r["step"]["rows"], us_per_step=round(r["us"], 2),
+                                   us_per_step_dist=r["dist"],
                                    hbm_gbs=round(r["bytes"] / r["us"] / 1e3, 1),
                                    frac_of_8tbs=round(r["bytes"] / r["us"] / 1e3 / NOMINAL_HBM_GBS, 4),
                                    bytes_per_step=int(r["bytes"]), d_hit=r["d_hit"])
@@ -700,7 +771,7 @@ def main():
         t = NCU_TRAFFIC.get((args.workload, top))
         if t is not None and t[1] == _gemm_source_hash():
             roof["traffic"] = t[0]
-            roof["traffic_source"] = "profiles/expert_gate_up_full_r48.md (ncu, one launch)"
+            roof["traffic_source"] = "ncu capture of one launch"
     total_prof = sum(prof.values())
     gbs = res["bytes"] / res["us"] / 1e3
     line = dict(
@@ -715,6 +786,7 @@ def main():
                        f"copies ({res['bytes'] / 1e6:.0f} MB touched per step, L2 {l2 / 1e6:.0f} MB)",
                     graph="each step replayed from a one-step CUDA graph of programmatically "
                           "serialised launches"),
+        us_per_step_dist=res["dist"],
         hbm_gbs=round(gbs, 1), frac_of_8tbs=round(gbs / NOMINAL_HBM_GBS, 4),
         frac_of_measured_copy=round(gbs / peak, 4), bytes_per_step=int(res["bytes"]),
         d_hit=res["d_hit"],
@@ -727,7 +799,7 @@ def main():
         gpu_launches=res["launches"],
     )
     if rank == 0 and world == 1 and not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(res)
+        line["cpu_baseline"] = cpu_baseline(dev)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

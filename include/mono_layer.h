@@ -53,7 +53,10 @@ enum {
 enum {
   MONO_STATUS_UNMAPPED_PAGE = 1, /* a block-table entry was outside [0, kv_num_blocks) */
   MONO_STATUS_WAIT_TIMEOUT = 2,  /* a pipeline wait ran past its time budget */
-  MONO_STATUS_BAD_ROUTE = 4      /* routing metadata out of range */
+  MONO_STATUS_BAD_ROUTE = 4,     /* routing metadata out of range */
+  MONO_STATUS_F16_RANGE = 8      /* an activation copied to f16 for the tensor cores was
+                                    beyond +-65504 and was saturated there (the step's
+                                    result then differs from the unsaturated layer) */
 };
 
 /*
@@ -250,17 +253,20 @@ int mono_layer_set_profile_events(mono_layer_t *h, void *const *events, int n_ev
  * MONO_NOALLOC_SCRATCH_BYTES on every device that loads it, held until the process exits.
  *
  * q: bf16 [rows, n_q_heads * head_dim] (device); o: f16 [rows, n_q_heads * head_dim]
- * (device, written: each value is the bf16-rounded attention output); the cache view,
- * positions, row_req and block table as in mono_step_args; only the attention fields of
- * `spec` are read.  The caller owns every buffer.
- * Errors: MONO_ERR_TOO_MANY_ROWS when rows > 48 or when rows * n_q_heads * (head_dim + 2)
- * * 4 bytes times the fewest splits the window allows exceeds the fixed scratch; the other
- * codes as for a step.  The first call on each device looks the array's device address up
- * (with that device current) and raises two kernels' shared-memory limits; make that first
- * call before any stream capture.  Every call shares the one array and clears its counters
+ * (device, written: each value is the bf16-rounded attention output); both 16-byte
+ * aligned; the cache view, positions, row_req and block table as in mono_step_args; only
+ * the attention fields of `spec` are read.  The caller owns every buffer.
+ * The window is split into S = ceil(max(causal ? window : swa_width, window) / 128) parts,
+ * as in a step.  Errors: MONO_ERR_TOO_MANY_ROWS when rows > 48, or when S > 1 and the split
+ * partials, rows * n_q_heads * S * (head_dim + 4) * 4 bytes, exceed the scratch less its
+ * 8 KB header; MONO_ERR_BAD_ALIGNMENT for q, o or the cache view not 16-byte aligned; the
+ * other codes as for a step, all returned before anything is enqueued.  The first call on
+ * each device looks the array's device address up (with that device current) and raises
+ * two kernels' shared-memory limits; make that first call before any stream capture.  Every call shares the one array and clears its counters
  * and status word on `stream` first: calls whose work overlaps on the GPU (other streams,
  * other threads) race on it and must be serialised by the caller.  Unmapped pages are
- * skipped; their status bit is not reported by this entry point.
+ * skipped and their status bit is not reported by this entry point, so a caller must
+ * check its block table before the call.
  */
 #define MONO_NOALLOC_SCRATCH_BYTES (4u << 20)
 int mono_attention_noalloc(const mono_layer_spec *spec, const void *q, void *o,

@@ -19,7 +19,7 @@ ERRORS = {
     -4: "MONO_ERR_BAD_ALIGNMENT", -5: "MONO_ERR_BAD_KV_VIEW", -6: "MONO_ERR_UNSUPPORTED_DEVICE",
     -7: "MONO_ERR_CUDA", -8: "MONO_ERR_OUT_OF_MEMORY", -9: "MONO_ERR_DEVICE_STATUS",
 }
-STATUS_UNMAPPED_PAGE, STATUS_WAIT_TIMEOUT, STATUS_BAD_ROUTE = 1, 2, 4
+STATUS_UNMAPPED_PAGE, STATUS_WAIT_TIMEOUT, STATUS_BAD_ROUTE, STATUS_F16_RANGE = 1, 2, 4, 8
 
 BUF = dict(xn=0, qkv=1, qlatn=2, kvn=3, q=4, o=5, oa=6, h=7, u=8, logits=9, topk_idx=10,
            topk_w=11, slot_pos=12, ts=13, ys=14, tr=15, yr=16)

@@ -15,6 +15,7 @@ namespace mono {
 constexpr int ST_UNMAPPED_PAGE = 1;
 constexpr int ST_WAIT_TIMEOUT = 2;
 constexpr int ST_BAD_ROUTE = 4;
+constexpr int ST_F16_RANGE = 8;
 
 // A pipeline wait that takes longer than this is treated as a fault (normal waits are
 // microseconds).
@@ -266,6 +267,16 @@ __device__ __forceinline__ float round_bf16(float v) {
   return __bfloat162float(__float2bfloat16_rn(v));
 }
 __device__ __forceinline__ __half bf16_as_f16(float v) { return __float2half_rn(round_bf16(v)); }
+// A bf16 value bound for an f16 tensor-core operand: magnitudes above f16's largest finite
+// value are saturated to +-65504 and raise ST_F16_RANGE (below 2^-14 the copy is an f16
+// subnormal, within 2^-25 of the value: no flag).  NaN passes through.
+__device__ __forceinline__ float f16_range(float v, int* status) {
+  if (fabsf(v) > 65504.0f) {
+    if (status) atomicOr(status, ST_F16_RANGE);
+    v = copysignf(65504.0f, v);
+  }
+  return v;
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -310,6 +321,13 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
 __device__ __forceinline__ uint32_t pack_f16x2(float a, float b) {
   const __half2 h = __halves2half2(__float2half_rn(a), __float2half_rn(b));
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+// pack_f16x2 of two bf16 values through f16_range.
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float a, float b, int* status) {
+  return pack_f16x2(f16_range(a, status), f16_range(b, status));
+}
+__device__ __forceinline__ __half bf16_as_f16_sat(float v, int* status) {
+  return __float2half_rn(f16_range(round_bf16(v), status));
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);

@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(AttnArgs a) {
     if (h < hpg) {
       float f[8];
       bf16x8_to_f32(*reinterpret_cast<const uint4*>(a.q + (size_t)r * QW + (h0 + h) * DH + c * 8), f);
-      o = make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
-                     pack_f16x2(f[6], f[7]));
+      o = make_uint4(pack_f16x2_sat(f[0], f[1], a.status), pack_f16x2_sat(f[2], f[3], a.status),
+                     pack_f16x2_sat(f[4], f[5], a.status), pack_f16x2_sat(f[6], f[7], a.status));
     }
     *reinterpret_cast<uint4*>(qs + h * L::QS + c * 8) = o;
   }
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(AttnArgs a) {
       if (S == 1) {
         const float il = 1.0f / s_l[h];
         *reinterpret_cast<uint32_t*>(a.o + (size_t)r * QW + (h0 + h) * DH + d) =
-            pack_f16x2(round_bf16(v0 * il), round_bf16(v1 * il));
+            pack_f16x2_sat(round_bf16(v0 * il), round_bf16(v1 * il), a.status);
       } else {
         float* part = a.part + (((size_t)r * a.n_q + h0 + h) * S + sp) * PW;
         *reinterpret_cast<float2*>(part + ATTN_PART_HEAD + d) = make_float2(v0, v1);
@@ -263,8 +263,8 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(AttnArgs a) {
       }
     }
     *reinterpret_cast<uint2*>(a.o + (size_t)r * QW + (h0 + h) * DH + d) =
-        make_uint2(pack_f16x2(round_bf16(n0 / den), round_bf16(n1 / den)),
-                   pack_f16x2(round_bf16(n2 / den), round_bf16(n3 / den)));
+        make_uint2(pack_f16x2_sat(round_bf16(n0 / den), round_bf16(n1 / den), a.status),
+                   pack_f16x2_sat(round_bf16(n2 / den), round_bf16(n3 / den), a.status));
   }
   if (tid == 0) *ctr = 0;
 }

@@ -75,10 +75,14 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(NormArgs a) {
       bf16x8_to_f32(xv[c], f);
       bf16x8_to_f32(gv[c], g);
       uint4 o;
-      o.x = pack_f16x2(round_bf16(f[0] * inv * g[0]), round_bf16(f[1] * inv * g[1]));
-      o.y = pack_f16x2(round_bf16(f[2] * inv * g[2]), round_bf16(f[3] * inv * g[3]));
-      o.z = pack_f16x2(round_bf16(f[4] * inv * g[4]), round_bf16(f[5] * inv * g[5]));
-      o.w = pack_f16x2(round_bf16(f[6] * inv * g[6]), round_bf16(f[7] * inv * g[7]));
+      o.x = pack_f16x2_sat(round_bf16(f[0] * inv * g[0]), round_bf16(f[1] * inv * g[1]),
+                          a.status);
+      o.y = pack_f16x2_sat(round_bf16(f[2] * inv * g[2]), round_bf16(f[3] * inv * g[3]),
+                          a.status);
+      o.z = pack_f16x2_sat(round_bf16(f[4] * inv * g[4]), round_bf16(f[5] * inv * g[5]),
+                          a.status);
+      o.w = pack_f16x2_sat(round_bf16(f[6] * inv * g[6]), round_bf16(f[7] * inv * g[7]),
+                          a.status);
       *reinterpret_cast<uint4*>(y + i) = o;
     }
   }
@@ -149,10 +153,14 @@ __global__ void __launch_bounds__(NORM_THREADS) qkv_norm_insert_kernel(QkvNormIn
       bf16x8_to_f32(qv[c], f);
       bf16x8_to_f32(qg[c], g);
       uint4 o;
-      o.x = pack_f16x2(round_bf16(f[0] * invq * g[0]), round_bf16(f[1] * invq * g[1]));
-      o.y = pack_f16x2(round_bf16(f[2] * invq * g[2]), round_bf16(f[3] * invq * g[3]));
-      o.z = pack_f16x2(round_bf16(f[4] * invq * g[4]), round_bf16(f[5] * invq * g[5]));
-      o.w = pack_f16x2(round_bf16(f[6] * invq * g[6]), round_bf16(f[7] * invq * g[7]));
+      o.x = pack_f16x2_sat(round_bf16(f[0] * invq * g[0]), round_bf16(f[1] * invq * g[1]),
+                          a.status);
+      o.y = pack_f16x2_sat(round_bf16(f[2] * invq * g[2]), round_bf16(f[3] * invq * g[3]),
+                          a.status);
+      o.z = pack_f16x2_sat(round_bf16(f[4] * invq * g[4]), round_bf16(f[5] * invq * g[5]),
+                          a.status);
+      o.w = pack_f16x2_sat(round_bf16(f[6] * invq * g[6]), round_bf16(f[7] * invq * g[7]),
+                          a.status);
       *reinterpret_cast<uint4*>(a.qlatn + (size_t)r * a.q_rank + i) = o;
     }
   }

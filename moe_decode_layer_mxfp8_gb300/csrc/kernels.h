@@ -46,6 +46,7 @@ struct NormArgs {
   int resid_ld = 0;
   __nv_bfloat16* sum_out = nullptr;
   int sum_ld = 0;
+  int* status = nullptr;  // f16 range bit of the normed output
 };
 
 struct QkvNormInsertArgs {

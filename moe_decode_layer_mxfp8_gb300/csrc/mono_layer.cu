@@ -630,8 +630,10 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
 
   // ---------------------------------------------------------------- K1: attention front
   TRY(run([&] {
-    return launch_rmsnorm(L, {x, H, (const __nv_bfloat16*)h->w.attn_norm, H, s.eps,
-                              h->buf<__half>(MONO_BUF_XN), H}, R);
+    NormArgs n = {x, H, (const __nv_bfloat16*)h->w.attn_norm, H, s.eps,
+                  h->buf<__half>(MONO_BUF_XN), H};
+    n.status = h->status;
+    return launch_rmsnorm(L, n, R);
   }));
   TRY(run([&] {
     return dense_launch(h, D_WQKV, R, h->buf<__half>(MONO_BUF_XN), H, EPI_BF16,
@@ -707,6 +709,7 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
   MoeIn m = {};
   m.seam = {h->buf<__nv_bfloat16>(MONO_BUF_H), H, (const __nv_bfloat16*)h->w.ffn_norm, H, s.eps,
             h->buf<__half>(MONO_BUF_U), H};
+  m.seam.status = h->status;
   m.x = x;
   m.positions = a->positions;
   m.R = R;
@@ -733,6 +736,7 @@ int mono_ffn_step(mono_layer_t* h, const mono_ffn_args* a, void* stream_ptr) {
             (const __nv_bfloat16*)h->w.ffn_norm, H, s.eps, h->buf<__half>(MONO_BUF_U), H,
             reinterpret_cast<const __nv_bfloat16*>(a->attn_in), H,
             h->buf<__nv_bfloat16>(MONO_BUF_H), H};
+  m.seam.status = h->status;
   m.x = reinterpret_cast<const __nv_bfloat16*>(a->x_in);
   m.positions = a->positions;
   m.R = R;

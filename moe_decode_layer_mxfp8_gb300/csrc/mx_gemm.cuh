@@ -467,7 +467,7 @@ __device__ void store_rows(const GemmParams& p, const Item& it, const float* fin
           break;
         case EPI_F16:
         case EPI_SWIGLU_F16:
-          reinterpret_cast<__half*>(p.out)[o[u]] = bf16_as_f16(v[u]);
+          reinterpret_cast<__half*>(p.out)[o[u]] = bf16_as_f16_sat(v[u], p.status);
           break;
         case EPI_RESID_BF16:
           reinterpret_cast<__nv_bfloat16*>(p.out)[o[u]] = __float2bfloat16_rn(r[u] + v[u]);
@@ -507,7 +507,7 @@ __device__ __forceinline__ void store_value(const GemmParams& p, int orow, int c
       break;
     case EPI_F16:
     case EPI_SWIGLU_F16:
-      reinterpret_cast<__half*>(p.out)[o] = bf16_as_f16(v);
+      reinterpret_cast<__half*>(p.out)[o] = bf16_as_f16_sat(v, p.status);
       break;
     case EPI_RESID_BF16:
       reinterpret_cast<__nv_bfloat16*>(p.out)[o] = __float2bfloat16_rn(
@@ -656,7 +656,7 @@ __device__ void owner_epilogue(const GemmParams& p, const Item& it, const float*
           break;
         case EPI_F16:
         case EPI_SWIGLU_F16:
-          reinterpret_cast<__half*>(p.out)[o[u]] = bf16_as_f16(v[u]);
+          reinterpret_cast<__half*>(p.out)[o[u]] = bf16_as_f16_sat(v[u], p.status);
           break;
         case EPI_RESID_BF16:
           reinterpret_cast<__nv_bfloat16*>(p.out)[o[u]] = __float2bfloat16_rn(r[u] + v[u]);

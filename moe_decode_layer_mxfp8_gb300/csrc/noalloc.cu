@@ -84,7 +84,10 @@ extern "C" int mono_attention_noalloc(const mono_layer_spec* s, const void* q, v
   if (s->window < 1 || s->window > 1024 || s->swa_width < 1 || s->swa_width > 1024 ||
       s->block_size < 1 || s->kv_record_bytes < s->kv_dim + 4)
     return MONO_ERR_UNSUPPORTED_DIMS;
-  if (!aligned16(kv_cache) || kv_stride_tok % 16 || kv_stride_block % 16)
+  // q is read and o written in 16-byte vectors: a misaligned caller pointer is refused here
+  // instead of faulting in the kernel
+  if (!aligned16(q) || !aligned16(o) || !aligned16(kv_cache) || kv_stride_tok % 16 ||
+      kv_stride_block % 16)
     return MONO_ERR_BAD_ALIGNMENT;
   if (kv_stride_tok < s->kv_record_bytes || kv_stride_block < (int64_t)s->block_size * kv_stride_tok)
     return MONO_ERR_BAD_KV_VIEW;

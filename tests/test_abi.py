@@ -120,3 +120,26 @@ except RuntimeError as e:
 """
     out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True)
     assert out.stdout.strip() == "raised", out.stderr
+
+
+def test_noalloc_attention_refuses_misaligned_pointers_before_touching_the_device(built):
+    """mono_attention_noalloc reads q and writes o in 16-byte vectors: an unaligned q, o or
+    cache base is refused with MONO_ERR_BAD_ALIGNMENT on the host (these fake addresses are
+    never dereferenced, and no device is needed)."""
+    import gen
+    f = built.mono_attention_noalloc
+    f.restype = C.c_int
+    f.argtypes = [C.POINTER(m.Spec), C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                  C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_int64,
+                  C.c_void_p]
+    sp = m.make_spec(gen.spec_of("full_r48", max_rows=48))
+    ok, cache = 0x10000, 0x20000
+
+    def call(q, o, kv):
+        return f(C.byref(sp), q, o, ok, ok, ok, 4, 1, 8, kv, 128 * 528, 528, 4, None)
+
+    assert call(ok + 2, ok, cache) == -4     # q
+    assert call(ok, ok + 8, cache) == -4     # o
+    assert call(ok, ok, cache + 4) == -4     # cache base
+    assert f(C.byref(sp), ok, ok, ok, ok, ok, 4, 1, 8, cache, 128 * 528, 520, 4, None) == -4  # stride
+    assert f(C.byref(sp), ok, ok, ok, ok, ok, 4, 1, 8, cache, 128 * 528 - 16, 528, 4, None) == -5

@@ -257,3 +257,34 @@ def test_all_pad_rows_pass_x_through(name):
     torch.cuda.synchronize()
     assert layer.status() == 0
     assert np.array_equal(out2.cpu().view(torch.int16).numpy().view(np.uint16), g["out"])
+
+
+def test_f16_operand_overflow_saturates_and_raises_status():
+    """wo_a's E8M0 block scales raised by 2^20: its output oa (copied to f16 as wo_b's
+    tensor-core operand) then lies far beyond f16's range.  The copies saturate at +-65504
+    and raise MONO_STATUS_F16_RANGE instead of becoming infinities; the step's output stays
+    finite and the next normal step is unaffected."""
+    _need_gpu()
+    import moe_decode_layer_mxfp8_gb300 as m
+    spec, wn, sn, g, layer, wd, sd = _case("small_r11")
+    big = dict(wd)
+    big["wo_a_s"] = (wd["wo_a_s"].to(torch.int32) + 20).clamp(max=254).to(torch.uint8)
+    loud = m.Layer(spec, big)
+    out = torch.empty_like(sd["x"])
+    loud.step(sd["x"], out, sd["positions"], sd["row_req"], sd["block_table"], sd["kv_cache"].clone())
+    torch.cuda.synchronize()
+    st = loud.status(clear=True)
+    assert st & m.STATUS_F16_RANGE, st
+    rows, o_rank = sn["x"].shape[0], spec["o_rank"]
+    oa = loud.read("oa", rows * o_rank * 2).view(np.float16).reshape(rows, o_rank).astype(np.float32)
+    live = np.asarray(sn["positions"]) >= 0
+    assert np.isfinite(oa).all()
+    assert np.abs(oa[live]).max() == 65504.0
+    assert torch.isfinite(out.float()).all()
+    loud.close()
+    # the ordinary layer: no flag
+    out2 = torch.empty_like(sd["x"])
+    layer.status(clear=True)
+    layer.step(sd["x"], out2, sd["positions"], sd["row_req"], sd["block_table"], sd["kv_cache"].clone())
+    torch.cuda.synchronize()
+    assert layer.status() == 0

@@ -1,11 +1,20 @@
-"""The allocation-free attention entry point against the layer step's own attention.
+"""The allocation-free attention entry point, through the C ABI.
 
-mono_attention_noalloc serves callers that cannot allocate device memory (code running
-under CUDA-graph capture, runtimes without a device allocator): its scratch is a fixed
-array inside the library.  Here it is called twice in a row through the C ABI on the query
-and KV cache a layer step just used; both outputs must match the step's attention output
-within the tolerance of the stage parity tests (one bf16 ulp).  The second call shows that
-the shared scratch is cleared between calls.
+mono_attention_noalloc serves callers that cannot allocate device memory -- code running
+while a CUDA graph is being captured (an allocation would break the capture), runtimes
+without a device allocator, latency-critical host code that must not take the driver's
+allocation lock.  Its scratch (split partials, combine counters, status word) is one fixed
+array compiled into the library, shared by every call.
+
+Each case runs a layer step (which inserts the rows' KV records and leaves the step's
+query in its arena), then calls the entry point twice in a row on that query and cache.
+Both outputs must match the oracle's windowed attention on the same query and cache within
+the stage tolerance of the parity tests (one bf16 ulp plus 2e-3 of the rms), and must equal
+the layer step's own attention output bit for bit (the same kernel and split count, so any
+stale partial or counter left in the shared array by the first call would show in the
+second).  The windows span one split (small_r11, full_r48), two (the 192-wide non-causal
+draft rows of draft_r6) and three (the 300-key window of wide_r9, which also has a pad row).
+This file is collected last, so a stop at the first failure has run every other test first.
 """
 import ctypes as C
 
@@ -14,7 +23,9 @@ import pytest
 import torch
 
 import gen
+import oracle
 from tests.gpu_harness import bf16_ulp_check, f16_to_bf16_bits, to_device
+from tests.helpers import np_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -32,14 +43,22 @@ def _entry():
     return m, f
 
 
-@pytest.mark.parametrize("name", ["small_r11", "full_r48"])
-def test_noalloc_attention_matches_layer_step(name):
+def _splits(spec):
+    width = max(spec["window"] if spec["causal"] else spec["swa_width"], spec["window"])
+    return (width + 127) // 128
+
+
+@pytest.mark.parametrize("name,splits", [("small_r11", 1), ("wide_r9", 3), ("draft_r6", 2),
+                                         ("full_r48", 1)])
+def test_noalloc_attention_matches_oracle_and_layer_step(name, splits):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     m, f = _entry()
+    oracle.build()
     dev = torch.device("cuda")
     full = gen.WORKLOADS[name]["spec"]["hidden"] >= 4096
     spec, w, st = gen.make_workload(name, weight_device=dev if full else "cpu")
+    assert _splits(spec) == splits
     wd, sd = to_device(w, st, dev)
     layer = m.Layer(spec, wd)
     cache = sd["kv_cache"].clone()
@@ -49,7 +68,13 @@ def test_noalloc_attention_matches_layer_step(name):
     assert layer.status() == 0
     rows, QW = st["rows"], spec["n_q_heads"] * spec["head_dim"]
     o_step = f16_to_bf16_bits(layer.read("o", rows * QW * 2).view(np.float16).reshape(rows, QW))
+    q_bits = layer.read("q", rows * QW * 2).view(np.uint16).reshape(rows, QW)
     q_ptr, _ = layer.buffer("q")
+
+    # the oracle on the same query and the cache after the step's insert
+    _, sn = np_inputs({}, st)
+    rc, o_want = oracle.attention(spec, sn, q_bits, cache=cache.cpu().numpy())
+    assert rc == 0
 
     stream = torch.cuda.current_stream()
     sp = m.make_spec(spec)
@@ -62,7 +87,10 @@ def test_noalloc_attention_matches_layer_step(name):
         assert rc == 0, m.strerror(rc)
         torch.cuda.synchronize()
         got = f16_to_bf16_bits(o.cpu().numpy())
-        bf16_ulp_check(got, o_step, f"noalloc call {call}")
+        bf16_ulp_check(got, o_want, f"{name}: noalloc call {call} against the oracle")
+        assert np.array_equal(got, o_step), f"{name}: noalloc call {call} differs from the step"
+        pad = np.asarray(st["positions"]) < 0
+        assert not got[pad].any()
     layer.close()
 
 
