@@ -77,6 +77,22 @@ WORKLOADS = {
                               block_size=64, kv_record_bytes=144, eps=1e-6, swiglu_clamp=7.0,
                               routed_scale=2.5),
                     contexts=[400, 350, 900], rows_per_req=[3, 3, 2], pad_rows=1, seed=13),
+    # the smallest shapes of the FP4 tensor-core expert path (hidden and intermediate whole
+    # 512-element runs, more than 24 routed slots): 13 rows over 3 requests with a pad row,
+    # 64 experts top-8 (1 to a few rows per expert); and 20 identical rows top-4, which
+    # puts 20 rows on each of 4 experts (a full 16-row group and a ragged 4-row one)
+    "mid_r13": dict(spec=dict(hidden=1024, n_q_heads=16, head_dim=64, kv_dim=128, q_rank=256,
+                              o_rank=256, n_experts=64, topk=8, moe_inter=512,
+                              shared_inter=512, window=64, swa_width=64, causal=1,
+                              block_size=64, kv_record_bytes=144, eps=1e-6, swiglu_clamp=7.0,
+                              routed_scale=1.5),
+                    contexts=[200, 90, 500], rows_per_req=[5, 4, 3], pad_rows=1, seed=16),
+    "skew_r20": dict(spec=dict(hidden=1024, n_q_heads=16, head_dim=64, kv_dim=128, q_rank=256,
+                               o_rank=256, n_experts=32, topk=4, moe_inter=512,
+                               shared_inter=512, window=64, swa_width=64, causal=1,
+                               block_size=64, kv_record_bytes=144, eps=1e-6, swiglu_clamp=7.0,
+                               routed_scale=1.0),
+                     contexts=[300], rows_per_req=20, pad_rows=0, seed=17, repeat_input=True),
 }
 
 

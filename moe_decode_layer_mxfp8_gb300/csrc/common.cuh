@@ -169,6 +169,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            int w, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
@@ -260,6 +268,40 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t e) {
   return __uint_as_float(bits);
 }
 
+// ----------------------------------------------------- e2m1 term split of activations
+// The block-scaled FP4 tensor-core path takes an activation value v (a bf16 number) as a sum
+// of ACT_TERMS e2m1 numbers, each 32-element block of a term under its own E8M0 scale:
+// v = sum_t c_t * 2^(s_t - 127).  Term t's scale is the smallest power of two that brings
+// the block's remaining residual within +-6 (the largest e2m1 magnitude), the codes round
+// the residual to nearest (even), and the residual left after a term is exact in f32: every
+// value is a bf16 number and each term removes a leading part of its bits.  Eight terms
+// leave nothing of the layer's activations (each term shrinks a block's largest residual at
+// least threefold, usually far more); the products then equal those of the f16 path.
+constexpr int ACT_TERMS = 8;
+
+// Two f32 values rounded to nearest-even e2m1 (saturating at +-6) in one byte, lo in the low
+// nibble.
+__device__ __forceinline__ uint32_t e2m1x2_of(float lo, float hi) {
+  uint32_t out;
+  asm("{\n .reg .b8 t;\n .reg .b16 w;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n"
+      " mov.b16 w, {t, 0};\n cvt.u32.u16 %0, w;\n}"
+      : "=r"(out)
+      : "f"(hi), "f"(lo));
+  return out;
+}
+// E8M0 code of a term's scale: the smallest 2^(code - 127) with 6 * 2^(code - 127) >= a
+// (127 for a = 0), within 1..253.
+__device__ __forceinline__ uint32_t e2m1_term_code(float a) {
+  if (!(a > 0.0f)) return 127u;
+  const uint32_t b = __float_as_uint(a);
+  const int code = (int)((b >> 23) & 0xFF) - 2 + ((b & 0x7FFFFFu) > 0x400000u ? 1 : 0);
+  return (uint32_t)min(max(code, 1), 253);
+}
+__device__ __forceinline__ float e8m0_pow2(uint32_t code) { return __uint_as_float(code << 23); }
+__device__ __forceinline__ float e8m0_inv_pow2(uint32_t code) {
+  return __uint_as_float((254u - code) << 23);
+}
+
 // ----------------------------------------------------------------------- activations
 // The layer's activations are bf16 at every rounding point.  Tensor-core operands are
 // f16 copies of those bf16 values (exact for |v| in [2^-14, 65504]).
@@ -332,6 +374,66 @@ __device__ __forceinline__ __half bf16_as_f16_sat(float v, int* status) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+}  // namespace mono
+
+namespace mono {
+
+// The e2m1 term split of a 32-element block held 8 consecutive values per lane by an aligned
+// group of 4 lanes (all 32 lanes of the warp call it): words[t] = this lane's 8 codes of term
+// t (element 2i in the low nibble of byte i), codes[t] = the term's E8M0 scale code.
+__device__ __forceinline__ void split_terms_x8(const float (&v)[8], uint32_t (&words)[ACT_TERMS],
+                                               uint32_t (&codes)[ACT_TERMS]) {
+  float r[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) r[i] = v[i];
+#pragma unroll
+  for (int t = 0; t < ACT_TERMS; ++t) {
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(r[i]));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    const uint32_t code = e2m1_term_code(a);
+    const float inv = e8m0_inv_pow2(code), sc = e8m0_pow2(code);
+    uint32_t w = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w |= e2m1x2_of(r[2 * i] * inv, r[2 * i + 1] * inv) << (8 * i);
+    uint32_t h[4];
+    e2m1x8_to_f16x8(w, h);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 q = __half22float2(*reinterpret_cast<const __half2*>(&h[i]));
+      r[2 * i] -= q.x * sc;
+      r[2 * i + 1] -= q.y * sc;
+    }
+    words[t] = w;
+    codes[t] = code;
+  }
+}
+
+// The same split for a 32-element block held one value per lane by a whole warp: words[t]
+// = the codes of the 8-lane group this lane belongs to (lanes 8k .. 8k + 7 give bytes 0 .. 3
+// of word k), codes[t] = the term's scale code.
+__device__ __forceinline__ void split_terms_lane(float v, uint32_t (&words)[ACT_TERMS],
+                                                 uint32_t (&codes)[ACT_TERMS]) {
+  const int lane = threadIdx.x & 31;
+  float r = v;
+#pragma unroll
+  for (int t = 0; t < ACT_TERMS; ++t) {
+    const uint32_t code = e2m1_term_code(warp_max(fabsf(r)));
+    const uint32_t nib = e2m1x2_of(r * e8m0_inv_pow2(code), 0.0f) & 0xFu;
+    uint32_t h[4];
+    e2m1x8_to_f16x8(nib, h);
+    r -= __low2float(*reinterpret_cast<const __half2*>(&h[0])) * e8m0_pow2(code);
+    uint32_t w = nib << (4 * (lane & 7));
+    w |= __shfl_xor_sync(0xffffffffu, w, 1);
+    w |= __shfl_xor_sync(0xffffffffu, w, 2);
+    w |= __shfl_xor_sync(0xffffffffu, w, 4);
+    words[t] = w;
+    codes[t] = code;
+  }
 }
 
 }  // namespace mono

@@ -1,0 +1,546 @@
+// Routed-expert GEMMs of large steps on the 5th-generation tensor cores ("Mono decode layer
+// for DeepSeek-V4.1-Flash on MI355X", launch table K2: "MXFP4 experts"; section Design: MXFP4
+// routed experts with 1x32 E8M0 scales, read in place).
+//
+// tcgen05.mma kind::mxf4 (block-scaled, scale_vec::2X) multiplies the expert's e2m1 weights,
+// TMA-loaded as stored (packed, 128-byte swizzle) with their E8M0 scales, by the routed rows'
+// activations.  An activation row enters as the ACT_TERMS e2m1 terms of its split (see
+// split_terms_x8 in common.cuh): row j of the item is MMA columns 8j .. 8j + 7, one per term,
+// and the epilogue adds a row's eight accumulator columns in term order.  One M = 128, K = 64
+// MMA covers 4 KB of packed weights whatever N (<= 64), so the weight stream, not the tensor
+// core, sets the pace.
+//
+// Two CTAs per SM, six warps each: warp 0 loads (TMA for the weight tiles and their scale
+// boxes, bulk copies for the term rows and term scales); warp 1 turns each stage's scales
+// into the TMEM scale images (all lanes) and issues the copies and MMAs (one elected lane)
+// into a double-buffered TMEM accumulator; warps 2-5 (one per TMEM lane quadrant) run the
+// epilogue.  (A CTA's stage costs some 900 cycles of issue and bookkeeping across its two
+// pipeline warps, so one pipeline per SM falls short of the SM's share of HBM bandwidth; two
+// reach it.)  Items are (hit expert, group of up to 8 routed rows, weight tile), handed out
+// by a per-launch counter, largest groups first.
+// gate_up tiles are 64 gate rows with the 64 up rows they pair with; the epilogue forms
+// SwiGLU and writes t (f16) and t's term split for the down GEMM.  Every wait is bounded.
+#include <algorithm>
+
+#include "kernels.h"
+
+namespace mono {
+namespace {
+
+constexpr int TC_M = 128;                    // weight rows per tile (the MMA's M)
+constexpr int TC_KC = 256;                   // K elements per stage (128 packed bytes a row)
+constexpr int TC_ROWS = 8;                   // routed rows per item
+constexpr int TC_NMAX = TC_ROWS * ACT_TERMS; // MMA columns at most
+constexpr int TC_THREADS = 192;
+constexpr int TC_CTAS_PER_SM = 2;           // two pipelines per SM (shared memory, TMEM halves)
+constexpr int TERM_ROW = 128;                // bytes of one term row per stage
+constexpr int TERM_SC = ACT_TERMS * 8;       // term-scale bytes of one routed row per stage
+constexpr int A_BYTES = TC_M * 128;
+constexpr int B_BYTES = TC_NMAX * TERM_ROW;
+constexpr int SA_BYTES = TC_M * 16;          // weight scale boxes: 16 bytes a row
+constexpr int SB_BYTES = TC_ROWS * TERM_SC;
+constexpr int IMG = 512;                     // one TMEM scale image: 32 lanes x 16 bytes
+constexpr int A_OFF = 0, B_OFF = A_BYTES, SA_OFF = B_OFF + B_BYTES, SB_OFF = SA_OFF + SA_BYTES;
+constexpr int IMG_OFF = SB_OFF + SB_BYTES;   // A word 0, A word 1, B word 0, B word 1
+constexpr int STAGE = (IMG_OFF + 4 * IMG + 1023) / 1024 * 1024;
+constexpr int NSTAGE = 3;
+constexpr int XCH_OFF = NSTAGE * STAGE;      // gate_up: the up rows' values for the gate warps,
+constexpr int XCH_BYTES = 2 * 64 * TC_ROWS * 4;  // one buffer per accumulator
+constexpr int SMEM_BYTES = XCH_OFF + XCH_BYTES + 1024;  // + alignment slack
+static_assert(STAGE % 1024 == 0, "stage buffers stay 1024-aligned for the 128-byte swizzle");
+// TMEM: two accumulators of TC_NMAX columns, then 16 scale columns per ring stage
+constexpr int SC_COL = 2 * TC_NMAX;
+constexpr int TMEM_COLS = 256;
+static_assert(SC_COL + 16 * NSTAGE <= TMEM_COLS, "TMEM columns");
+static_assert(TMEM_COLS * TC_CTAS_PER_SM <= 512, "the co-resident CTAs' TMEM fits the SM's");
+constexpr int MAX_GROUPS = MAX_SLOTS;        // row groups at most (<= routed slots)
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Descriptor of a scale image (32 rows x 16 B, no swizzle).
+__device__ __forceinline__ uint64_t desc_img(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) |
+         ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Copies a 32-lane x 16-byte image into TMEM columns [taddr, taddr + 4) of every lane
+// quadrant: lane l, column g of the image holds row (or MMA column) l + 32 g's four scale
+// bytes, byte b for K-block b of the 128-element half-stage the image covers.
+__device__ __forceinline__ void tc_cp_img(uint32_t taddr, const void* img) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr),
+               "l"(desc_img(smem_u32(img)))
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.b32 q, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], q;\n}"
+      ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+// Arrives on the mbarrier once every MMA / copy this thread has issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tc_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// True in one lane of the (converged) warp: the thread that issues the tensor-core work.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t r;
+  asm volatile("{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n selp.u32 %0, 1, 0, e;\n}"
+               : "=r"(r));
+  return r != 0;
+}
+// A bounded wait whose outcome the whole warp shares (every lane calls it).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          volatile int* abort) {
+  return __all_sync(0xffffffffu, pipe_wait(bar, parity, status, abort));
+}
+
+// Items of a launch: hit expert d owns row groups [gpre[d], gpre[d + 1]) (ceil(rows / 16)
+// each) and items [gpre[d] * n_tiles, gpre[d + 1] * n_tiles), tile fastest.
+struct TcRoute {
+  int n_hit;
+  int e[MAX_EXPERTS], off[MAX_EXPERTS], cnt[MAX_EXPERTS];
+  int gpre[MAX_EXPERTS + 1];
+  uint8_t gexp[MAX_GROUPS];  // hit expert of each row group
+  int rowmap[MAX_SLOTS];     // gate_up: sorted slot -> activation row
+};
+static_assert(MAX_EXPERTS <= 256, "gexp holds hit-expert indices in a byte");
+
+struct TcItem {
+  int e, tile, slot0, n;  // expert, weight tile, first sorted slot, routed rows (1 .. 16)
+};
+__device__ __forceinline__ TcItem tc_item(const TcRoute& rt, int n_tiles, int q) {
+  const int g = q / n_tiles;
+  const int d = rt.gexp[g];
+  const int lg = g - rt.gpre[d];
+  TcItem it;
+  it.e = rt.e[d];
+  it.tile = q - g * n_tiles;
+  it.slot0 = rt.off[d] + lg * TC_ROWS;
+  it.n = min(TC_ROWS, rt.cnt[d] - lg * TC_ROWS);
+  return it;
+}
+
+template <bool GU>
+__global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM)
+    expert_tc_kernel(const __grid_constant__ CUtensorMap wmap,
+                     const __grid_constant__ CUtensorMap smap, const ExpertTcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full[NSTAGE], empty[NSTAGE], tfull[2], tempty[2], drain;
+  __shared__ __align__(8) uint64_t xfull[2], xempty[2];  // gate_up: the up-value exchange
+  __shared__ TcRoute rt;
+  __shared__ int slot_q[NSTAGE], acc_q[2];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  volatile int* abort = &s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nck = p.K / TC_KC;
+
+  if (tid == 0) {
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&full[s], 1);   // the producer's expect_tx arrival; the copies complete_tx
+      mbar_init(&empty[s], 1);  // the MMA thread's commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 2);   // the item index published, then the MMAs' commit
+      mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+      mbar_init(&xfull[b], 64);  // every lane of the two up-row warps
+      mbar_init(&xempty[b], 64); // every lane of the two gate-row warps
+    }
+    mbar_init(&drain, 1);
+    *abort = 0;
+    fence_mbar_init();
+    prefetch_tmap(&wmap);
+    prefetch_tmap(&smap);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&s_tmem)),
+                 "n"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  pdl_trigger();
+  pdl_wait();
+
+  // routing metadata (written by the top-k kernel), checked, and the row groups
+  int n_hit = p.route->n_hit;
+  if (n_hit < 0 || n_hit > MAX_EXPERTS) {
+    if (tid == 0) atomicOr(p.status, ST_BAD_ROUTE);
+    n_hit = 0;
+  }
+  // (staged in the ring's memory, which the pipeline does not use yet)
+  int* ue = reinterpret_cast<int*>(smem);
+  int* uoff = ue + MAX_EXPERTS;
+  int* ucnt = uoff + MAX_EXPERTS;
+  for (int d = tid; d < n_hit; d += TC_THREADS) {
+    int e = p.route->hit_e[d], off = p.route->hit_off[d], cnt = p.route->hit_cnt[d];
+    if (e < 0 || e >= p.n_experts || cnt < 1 || off < 0 || off + cnt > p.n_slots) {
+      atomicOr(p.status, ST_BAD_ROUTE);
+      e = 0, off = 0, cnt = 1;
+    }
+    ue[d] = e, uoff[d] = off, ucnt[d] = cnt;
+  }
+  __syncthreads();
+  // the hit experts in decreasing row count (ties in expert order), so that the items of the
+  // largest groups, which stream slowest, are handed out first and the launch ends on short
+  // ones
+  for (int d = tid; d < n_hit; d += TC_THREADS) {
+    const int cd = ucnt[d];
+    int rank = 0;
+    for (int k = 0; k < n_hit; ++k) {
+      const int ck = ucnt[k];
+      rank += (ck > cd) | ((ck == cd) & (k < d));
+    }
+    rt.e[rank] = ue[d], rt.off[rank] = uoff[d], rt.cnt[rank] = cd;
+  }
+  if constexpr (GU) {
+    for (int i = tid; i < p.n_slots; i += TC_THREADS) {
+      int r = p.rowmap[i];
+      if (r < 0 || r >= p.act_rows) {
+        atomicOr(p.status, ST_BAD_ROUTE);
+        r = 0;
+      }
+      rt.rowmap[i] = r;
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {  // row-group prefix over the hit experts
+    int carry = 0;
+    for (int d0 = 0; d0 < n_hit; d0 += 32) {
+      const int d = d0 + lane;
+      const int v = d < n_hit ? (rt.cnt[d] + TC_ROWS - 1) / TC_ROWS : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (d < n_hit) rt.gpre[d] = carry + x - v;
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) {
+      rt.gpre[n_hit] = carry;
+      rt.n_hit = n_hit;
+    }
+  }
+  __syncthreads();
+  for (int d = tid; d < n_hit; d += TC_THREADS)
+    for (int g = rt.gpre[d]; g < rt.gpre[d + 1] && g < MAX_GROUPS; ++g) rt.gexp[g] = (uint8_t)d;
+  __syncthreads();
+  const int n_items = min(rt.gpre[n_hit], MAX_GROUPS) * p.n_tiles;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------------------- producer
+    int iter = 0;
+    int q = 0;
+    if (lane == 0) q = atomicAdd(p.item_next, 1);
+    q = __shfl_sync(0xffffffffu, q, 0);
+    while (q < n_items) {
+      int qn = 0;
+      if (lane == 0) qn = atomicAdd(p.item_next, 1);
+      const TcItem it = tc_item(rt, p.n_tiles, q);
+      int arow = 0;
+      if (GU && lane < it.n) arow = rt.rowmap[it.slot0 + lane];
+      const uint32_t tx = A_BYTES + SA_BYTES + it.n * (ACT_TERMS * TERM_ROW + TERM_SC);
+      for (int c = 0; c < nck; ++c, ++iter) {
+        const int s = iter % NSTAGE;
+        if (!warp_wait(&empty[s], ((iter / NSTAGE) & 1) ^ 1, p.status, abort)) goto producer_done;
+        uint8_t* st = smem + s * STAGE;
+        if (elect_one()) {
+          if (c == 0) slot_q[s] = q;  // published by the arrival below
+          mbar_arrive_expect_tx(&full[s], tx);
+          if constexpr (GU) {  // the tile's 64 gate rows, then the 64 up rows I further
+            tma_load_4d(st + A_OFF, &wmap, c * 128, it.tile * 64, 0, it.e, &full[s]);
+            tma_load_4d(st + SA_OFF, &smap, (c * 8) & ~15, it.tile * 64, 0, it.e, &full[s]);
+          } else {
+            const int row = it.e * p.rows_per_mat + it.tile * TC_M;
+            tma_load_2d(st + A_OFF, &wmap, c * 128, row, &full[s]);
+            tma_load_2d(st + SA_OFF, &smap, (c * 8) & ~15, row, &full[s]);
+            // the item's slots are consecutive: their term rows and scales, one copy each
+            const size_t rc = (size_t)c * p.n_slots + it.slot0;
+            bulk_load_g2s(st + B_OFF, p.bterms + rc * (ACT_TERMS * TERM_ROW),
+                          it.n * (ACT_TERMS * TERM_ROW), &full[s]);
+            bulk_load_g2s(st + SB_OFF, p.bscales + rc * TERM_SC, it.n * TERM_SC, &full[s]);
+          }
+        }
+        __syncwarp();
+        if (GU && lane < it.n) {  // gathered rows of u: one pair of copies per row
+          const size_t rc = (size_t)arow * nck + c;
+          bulk_load_g2s(st + B_OFF + lane * (ACT_TERMS * TERM_ROW),
+                        p.bterms + rc * (ACT_TERMS * TERM_ROW), ACT_TERMS * TERM_ROW, &full[s]);
+          bulk_load_g2s(st + SB_OFF + lane * TERM_SC, p.bscales + rc * TERM_SC, TERM_SC, &full[s]);
+        }
+      }
+      q = __shfl_sync(0xffffffffu, qn, 0);
+    }
+    {  // the end: one more stage phase that carries no data, only the end mark
+      const int s = iter % NSTAGE;
+      if (!warp_wait(&empty[s], ((iter / NSTAGE) & 1) ^ 1, p.status, abort)) goto producer_done;
+      if (lane == 0) {
+        slot_q[s] = -1;
+        mbar_arrive(&full[s]);
+      }
+    }
+  producer_done:
+    if (lane == 0 && *abort) {  // let the copies already issued land before the CTA exits
+      for (int k = max(0, iter - NSTAGE); k < iter; ++k)
+        mbar_wait(&full[k % NSTAGE], (k / NSTAGE) & 1, p.status, 100000000ull);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ scale images + MMA issue
+    int iter = 0;
+    for (int li = 0;; ++li) {
+      const int b = li & 1;
+      int s = iter % NSTAGE;
+      if (!warp_wait(&full[s], (iter / NSTAGE) & 1, p.status, abort)) break;
+      const int q = slot_q[s];
+      if (!warp_wait(&tempty[b], ((li >> 1) & 1) ^ 1, p.status, abort)) break;
+      if (lane == 0) {
+        acc_q[b] = q;
+        mbar_arrive(&tfull[b]);  // publishes the item index (release)
+      }
+      if (q < 0) {
+        if (elect_one()) tc_commit(&tfull[b]);  // (the issuing thread's commits)
+        break;
+      }
+      const TcItem it = tc_item(rt, p.n_tiles, q);
+      const int ncol = (it.n * ACT_TERMS + 15) & ~15;
+      const uint32_t d0 = tmem + b * TC_NMAX;
+      const uint32_t idesc_base = (1u << 7) | (1u << 10) | ((uint32_t)(ncol >> 3) << 17) |
+                                  (1u << 23) | ((uint32_t)(TC_M >> 4) << 24);
+      bool ok = true;
+      for (int c = 0; c < nck; ++c, ++iter) {
+        s = iter % NSTAGE;
+        if (c > 0 && !warp_wait(&full[s], (iter / NSTAGE) & 1, p.status, abort)) {
+          ok = false;
+          break;
+        }
+        uint8_t* st = smem + s * STAGE;
+        // scale images.  A word w: lane l, column g = weight row l + 32 g's K-block scales
+        // 4w .. 4w + 3 of this stage, bytes (8c & 8) + 4w .. of the row's 16-byte box row.
+        // B word w: lane l, column g = MMA column n = l + 32 g, routed row n / 8's term n % 8.
+        {
+          const bool hi = (c & 1) != 0;  // the stage's scales are the box row's second half
+          uint32_t w0[4], w1[4];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint4 r = *reinterpret_cast<const uint4*>(st + SA_OFF + (lane + 32 * g) * 16);
+            w0[g] = hi ? r.z : r.x;
+            w1[g] = hi ? r.w : r.y;
+          }
+          *reinterpret_cast<uint4*>(st + IMG_OFF + lane * 16) =
+              make_uint4(w0[0], w0[1], w0[2], w0[3]);
+          *reinterpret_cast<uint4*>(st + IMG_OFF + IMG + lane * 16) =
+              make_uint4(w1[0], w1[1], w1[2], w1[3]);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int n = lane + 32 * g;
+            uint2 v = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);  // unused columns: scale 1
+            if (n < it.n * ACT_TERMS)
+              v = *reinterpret_cast<const uint2*>(st + SB_OFF + (n >> 3) * TERM_SC + (n & 7) * 8);
+            w0[g] = v.x;
+            w1[g] = v.y;
+          }
+          *reinterpret_cast<uint4*>(st + IMG_OFF + 2 * IMG + lane * 16) =
+              make_uint4(w0[0], w0[1], w0[2], w0[3]);
+          *reinterpret_cast<uint4*>(st + IMG_OFF + 3 * IMG + lane * 16) =
+              make_uint4(w1[0], w1[1], w1[2], w1[3]);
+        }
+        fence_proxy_async_shared();  // the images, before the tensor core's copies read them
+        __syncwarp();
+        const uint32_t sc = tmem + SC_COL + s * 16;
+        const uint32_t a0 = smem_u32(st + A_OFF), b0 = smem_u32(st + B_OFF);
+        if (elect_one()) {
+          tc_fence_after();
+          tc_cp_img(sc, st + IMG_OFF);
+          tc_cp_img(sc + 4, st + IMG_OFF + IMG);
+          tc_cp_img(sc + 8, st + IMG_OFF + 2 * IMG);
+          tc_cp_img(sc + 12, st + IMG_OFF + 3 * IMG);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {  // K = 64 each; scale bytes 2j % 4 of word j / 2
+            const uint32_t sf = 2u * (j & 1);
+            tc_mma_mxf4(d0, desc_sw128(a0 + 32 * j), desc_sw128(b0 + 32 * j),
+                        idesc_base | (sf << 4) | (sf << 29), sc + 4 * (j >> 1),
+                        sc + 8 + 4 * (j >> 1), (c > 0 || j > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (elect_one()) tc_commit(&tfull[b]);
+    }
+    // every MMA issued has completed before the accumulators and TMEM are released
+    if (elect_one()) {
+      tc_commit(&drain);
+      mbar_wait(&drain, 0, p.status, 100000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------------------- epilogue
+    const int quad = warp & 3;  // the TMEM lane quadrant this warp may read: tile rows 32 quad ..
+    for (int li = 0;; ++li) {
+      const int b = li & 1;
+      const uint32_t ph = (li >> 1) & 1;
+      float* xch = reinterpret_cast<float*>(smem + XCH_OFF) + b * 64 * TC_ROWS;  // [64][16]
+      if (!warp_wait(&tfull[b], ph, p.status, abort)) break;
+      tc_fence_after();
+      const int q = acc_q[b];
+      if (q < 0) break;
+      const TcItem it = tc_item(rt, p.n_tiles, q);
+      // this lane's weight row's value for each routed row: the sum of its eight term columns
+      float y[TC_ROWS];
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + b * TC_NMAX;
+#pragma unroll
+      for (int c4 = 0; c4 < TC_NMAX / 32; ++c4) {
+        if (c4 * 4 < it.n) {  // 32 columns = 4 routed rows
+          uint32_t r[32];
+          tc_ld32(taddr + c4 * 32, r);
+          tc_wait_ld();
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            float v = 0.0f;
+#pragma unroll
+            for (int t = 0; t < ACT_TERMS; ++t) v += __uint_as_float(r[jj * 8 + t]);
+            y[c4 * 4 + jj] = v;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[b]);
+      if constexpr (GU) {
+        // up rows (quadrants 2, 3) hand their values to the gate rows (quadrants 0, 1)
+        if (quad >= 2) {
+          if (!warp_wait(&xempty[b], ph ^ 1, p.status, abort)) break;
+#pragma unroll
+          for (int j = 0; j < TC_ROWS; ++j)
+            if (j < it.n) xch[((quad - 2) * 32 + lane) * TC_ROWS + j] = y[j];
+          mbar_arrive(&xfull[b]);
+        } else {
+          if (!warp_wait(&xfull[b], ph, p.status, abort)) break;
+          const int col = it.tile * 64 + quad * 32 + lane;  // t's column (down's K index)
+          const int kc = col / TC_KC, piece = (col % TC_KC) / 32;
+#pragma unroll 1
+          for (int j = 0; j < TC_ROWS; ++j) {
+            if (j >= it.n) break;
+            const size_t slot = (size_t)it.slot0 + j;
+            const float t = round_bf16(
+                swiglu_clamped(y[j], xch[(quad * 32 + lane) * TC_ROWS + j], p.clamp));
+            p.t16[slot * p.I + col] = bf16_as_f16_sat(t, p.status);
+            uint32_t words[ACT_TERMS], codes[ACT_TERMS];
+            split_terms_lane(t, words, codes);
+            const size_t base = ((size_t)kc * p.n_slots + slot) * ACT_TERMS;
+#pragma unroll
+            for (int tt = 0; tt < ACT_TERMS; ++tt) {
+              if ((lane & 7) == 0)
+                *reinterpret_cast<uint32_t*>(p.tterms + (base + tt) * TERM_ROW +
+                                             ((piece ^ tt) << 4) + (lane >> 3) * 4) = words[tt];
+              if (lane == 0) p.tscales[(base + tt) * 8 + piece] = (uint8_t)codes[tt];
+            }
+          }
+          mbar_arrive(&xempty[b]);  // (the up values are read before the lanes arrive)
+        }
+      } else {
+        const int col = it.tile * TC_M + quad * 32 + lane;
+#pragma unroll
+        for (int j = 0; j < TC_ROWS; ++j)
+          if (j < it.n) p.y[((size_t)it.slot0 + j) * p.rows_per_mat + col] = y[j];
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "n"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+cudaError_t expert_tc_prepare(int* ctas_per_sm) {
+  // the largest shared-memory carveout, so that TC_CTAS_PER_SM rings fit on an SM
+  cudaError_t e = cudaSuccess;
+  for (const void* k : {reinterpret_cast<const void*>(expert_tc_kernel<true>),
+                        reinterpret_cast<const void*>(expert_tc_kernel<false>)}) {
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+  }
+  // co-resident CTAs, from the kernel's registers and shared memory and the SM's totals (the
+  // runtime's occupancy query answers 1 for this kernel; two CTAs do share an SM, which the
+  // launch's time shows); never more than TC_CTAS_PER_SM, whose TMEM shares fill the SM's
+  int n = 0;
+  if (e == cudaSuccess) {
+    int dev = 0;
+    cudaDeviceProp pr;
+    cudaFuncAttributes fa[2];
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaGetDeviceProperties(&pr, dev);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa[0], expert_tc_kernel<true>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa[1], expert_tc_kernel<false>);
+    if (e == cudaSuccess) {
+      n = TC_CTAS_PER_SM;
+      for (const cudaFuncAttributes& a : fa) {
+        const size_t smem = SMEM_BYTES + a.sharedSizeBytes + pr.reservedSharedMemPerBlock;
+        const int regs = ((a.numRegs * 32 + 255) / 256 * 256) * (TC_THREADS / 32);
+        n = std::min(n, (int)std::min<size_t>(pr.sharedMemPerMultiprocessor / smem,
+                                               (size_t)(pr.regsPerMultiprocessor / regs)));
+      }
+    }
+  }
+  *ctas_per_sm = n;
+  return e;
+}
+
+cudaError_t launch_expert_tc(const Launch& L, bool gate_up, const CUtensorMap& wmap,
+                             const CUtensorMap& smap, const ExpertTcParams& p, int grid) {
+  if (p.K % TC_KC || (gate_up && (p.I % 64 || p.I % TC_KC)) || (!gate_up && p.rows_per_mat % TC_M) ||
+      !p.item_next || !p.route || p.n_slots > MAX_SLOTS)
+    return cudaErrorInvalidValue;
+  if (gate_up)
+    return launch_ex(L, dim3(grid), dim3(TC_THREADS), SMEM_BYTES, expert_tc_kernel<true>, wmap,
+                     smap, p);
+  return launch_ex(L, dim3(grid), dim3(TC_THREADS), SMEM_BYTES, expert_tc_kernel<false>, wmap,
+                   smap, p);
+}
+
+}  // namespace mono

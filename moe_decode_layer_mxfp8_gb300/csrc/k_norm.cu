@@ -84,6 +84,22 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(NormArgs a) {
       o.w = pack_f16x2_sat(round_bf16(f[6] * inv * g[6]), round_bf16(f[7] * inv * g[7]),
                           a.status);
       *reinterpret_cast<uint4*>(y + i) = o;
+      if (a.terms) {  // (a whole warp's chunks are in range or out of it: dim % 256 == 0)
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = round_bf16(f[j] * inv * g[j]);
+        uint32_t words[ACT_TERMS], codes[ACT_TERMS];
+        split_terms_x8(v, words, codes);
+        const int q = c * NORM_THREADS + tid;  // 8-element chunk of the row
+        const int piece = (q & 31) >> 2;       // 16-byte piece (= 32-element block) in its row
+        const size_t base = ((size_t)r * (a.dim / 256) + (q >> 5)) * ACT_TERMS;
+#pragma unroll
+        for (int t = 0; t < ACT_TERMS; ++t) {
+          *reinterpret_cast<uint32_t*>(a.terms + (base + t) * 128 + ((piece ^ t) << 4) +
+                                       (q & 3) * 4) = words[t];
+          if ((q & 3) == 0) a.term_scales[(base + t) * 8 + piece] = (uint8_t)codes[t];
+        }
+      }
     }
   }
 }

@@ -47,6 +47,12 @@ struct NormArgs {
   __nv_bfloat16* sum_out = nullptr;
   int sum_ld = 0;
   int* status = nullptr;  // f16 range bit of the normed output
+  // optional e2m1 term split of the normed row (the FP4 tensor-core experts' input; dim a
+  // multiple of 256): terms [rows][dim / 256][ACT_TERMS][128 B], each 128-byte term row
+  // stored with its 16-byte piece j at piece j ^ t (the 128-byte swizzle of shared-memory
+  // row t mod 8); term_scales [rows][dim / 256][ACT_TERMS][8 blocks]
+  uint8_t* terms = nullptr;
+  uint8_t* term_scales = nullptr;
 };
 
 struct QkvNormInsertArgs {
@@ -128,6 +134,41 @@ cudaError_t launch_topk(const Launch&, const TopkArgs&);
 cudaError_t launch_final(const Launch&, const FinalArgs&);
 // A bounded wait that runs out (see mono_layer_selftest_wait_timeout).
 cudaError_t launch_wait_timeout(cudaStream_t stream, int* status, unsigned long long budget_ns);
+
+// The routed-expert GEMMs of large steps on the FP4 tensor cores (k_expert_tc.cu).  Weight
+// maps (packed e2m1, 128-byte swizzle, 128-byte boxes along K): gate_up 4D [experts][2 halves]
+// [I rows][H / 2 bytes] with {128 B, 64 rows, 2 halves, 1} boxes (a tile's gate rows, then the
+// up rows they pair with); down 2D [experts * H rows][I / 2 bytes] with {128 B, 128 rows}
+// boxes.  Scale maps (E8M0, K / 32 bytes a row): the same shapes with 16-byte boxes along K.
+// The activations arrive as e2m1 term splits (ACT_TERMS terms, see common.cuh).
+struct ExpertTcParams {
+  int K;             // reduction length, a multiple of 256
+  int rows_per_mat;  // weight rows per expert: 2 I (gate_up) or H (down)
+  int I;             // gate_up: the intermediate width (tile t = gate rows 64t.., up rows I + 64t..)
+  int n_tiles;       // weight tiles per expert: I / 64 (gate_up) or H / 128 (down)
+  int n_experts;
+  int n_slots;       // routed (row, slot) pairs of the step
+  int act_rows;      // gate_up: rows of the activation split (the step's rows)
+  const int* rowmap; // gate_up: expert-sorted slot -> activation row
+  const RouteInfo* route;
+  int* item_next;    // the launch's work counter, zero at entry
+  // activation terms and their scales: gate_up [rows][K / 256][ACT_TERMS][128 B] and
+  // [rows][K / 256][ACT_TERMS][8]; down [K / 256][n_slots][ACT_TERMS][128 B] and
+  // [K / 256][n_slots][ACT_TERMS][8] (an item's consecutive slots are one run per stage)
+  const uint8_t* bterms;
+  const uint8_t* bscales;
+  __half* t16;             // gate_up: SwiGLU outputs, f16 [slots, I]
+  uint8_t* tterms;         // gate_up: their term split, in down's layout
+  uint8_t* tscales;
+  float* y;                // down: outputs f32 [slots, rows_per_mat]
+  float clamp;
+  int* status;
+};
+// raises the dynamic shared-memory limit; *ctas_per_sm = co-resident CTAs (the grid is that
+// times the SM count)
+cudaError_t expert_tc_prepare(int* ctas_per_sm);
+cudaError_t launch_expert_tc(const Launch&, bool gate_up, const CUtensorMap& wmap,
+                             const CUtensorMap& smap, const ExpertTcParams& p, int grid);
 
 // MX GEMM variants: fmt 8 (MXFP8) with nt in {1, 2, 4, 6}; fmt 4 (MXFP4) with nt 1.
 struct GemmVariant {

@@ -64,6 +64,12 @@ struct mono_layer {
   // the expert scale matrices as TMA maps when their rows are whole 16-byte runs
   CUtensorMap map_ex_gu_s, map_ex_d_s;
   bool sc_tma_gu = false, sc_tma_d = false;
+  // large steps: the routed experts on the FP4 tensor cores (64-row boxes), with the e2m1
+  // term splits of u and t in the arena
+  bool expert_tc = false;
+  int tc_ctas = 0;  // its grid: co-resident CTAs on every SM
+  CUtensorMap map_tc_gu, map_tc_d, map_tc_gu_s, map_tc_d_s;
+  uint8_t *u_terms = nullptr, *u_tscales = nullptr, *t_terms = nullptr, *t_tscales = nullptr;
   int ctas_gemm8[7] = {};  // by nt
   int ex_ctas = 0;      // persistent CTAs of the expert GEMM (large steps)
   int ex_clusters = 0;  // clusters of EXPERT_CLUSTER CTAs of the K-splitting expert GEMM
@@ -92,11 +98,12 @@ bool get_encoder() {
   return true;
 }
 
-// 2D byte tensor [rows, row_bytes] with 32-row x 128-byte boxes and 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, long long rows, long long row_bytes) {
+// 2D byte tensor [rows, row_bytes] with box_rows x 128-byte boxes and 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, long long rows, long long row_bytes,
+              int box_rows = BOX_ROWS) {
   cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-  cuuint32_t box[2] = {BOX_BYTES, BOX_ROWS};
+  cuuint32_t box[2] = {BOX_BYTES, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -106,13 +113,53 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long row_by
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-// 2D byte tensor [rows, row_bytes] of E8M0 scales with 16-byte x 32-row boxes, no swizzle;
+// Byte tensor of the given rank (dims innermost first, strides in bytes of dims 1..) with the
+// given box; false (and no map) on a misaligned base or stride.
+bool make_map_nd(CUtensorMap* m, const void* base, int rank, const long long* dims,
+                 const long long* strides, const int* box, bool swizzle128) {
+  if (!aligned16(base)) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = (cuuint64_t)dims[i];
+    b[i] = (cuuint32_t)box[i];
+    es[i] = 1;
+    if (i > 0) {
+      if (strides[i - 1] % 16) return false;
+      st[i - 1] = (cuuint64_t)strides[i - 1];
+    }
+  }
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, rank, const_cast<void*>(base), d, st, b, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The tensor-core expert path's maps (shapes in kernels.h, above ExpertTcParams).
+bool make_expert_tc_maps(mono_layer* h) {
+  const mono_layer_spec& s = h->spec;
+  const long long E = s.n_experts, H = s.hidden, I = s.moe_inter;
+  const long long gw[4] = {H / 2, I, 2, E}, gws[3] = {H / 2, I * H / 2, 2 * I * H / 2};
+  const long long gs[4] = {H / 32, I, 2, E}, gss[3] = {H / 32, I * H / 32, 2 * I * H / 32};
+  const int gwb[4] = {128, 64, 2, 1}, gsb[4] = {16, 64, 2, 1};
+  const long long dw[2] = {I / 2, E * H}, dws[1] = {I / 2};
+  const long long ds[2] = {I / 32, E * H}, dss[1] = {I / 32};
+  const int dwb[2] = {128, 128}, dsb[2] = {16, 128};
+  return make_map_nd(&h->map_tc_gu, h->w.ex_gu, 4, gw, gws, gwb, true) &&
+         make_map_nd(&h->map_tc_gu_s, h->w.ex_gu_s, 4, gs, gss, gsb, false) &&
+         make_map_nd(&h->map_tc_d, h->w.ex_d, 2, dw, dws, dwb, true) &&
+         make_map_nd(&h->map_tc_d_s, h->w.ex_d_s, 2, ds, dss, dsb, false);
+}
+
+// 2D byte tensor [rows, row_bytes] of E8M0 scales with 16-byte x box_rows boxes, no swizzle;
 // false (and no map) unless the rows are whole 16-byte runs at a 16-byte aligned base.
-bool make_scale_map(CUtensorMap* m, const void* base, long long rows, long long row_bytes) {
+bool make_scale_map(CUtensorMap* m, const void* base, long long rows, long long row_bytes,
+                    int box_rows = BOX_ROWS) {
   if (row_bytes % 16 || !aligned16(base)) return false;
   cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-  cuuint32_t box[2] = {16, BOX_ROWS};
+  cuuint32_t box[2] = {16, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -260,6 +307,8 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
   h->sc_tma_gu =
       make_scale_map(&h->map_ex_gu_s, wt->ex_gu_s, (long long)E * 2 * s.moe_inter, H / 32);
   h->sc_tma_d = make_scale_map(&h->map_ex_d_s, wt->ex_d_s, (long long)E * H, s.moe_inter / 32);
+  // the tensor-core expert path wants whole 256-element stages and 16-byte scale boxes
+  h->expert_tc = H % 512 == 0 && s.moe_inter % 512 == 0 && make_expert_tc_maps(h);
   const int width = std::max(s.causal ? s.window : s.swa_width, s.window);
   h->attn_min_splits = ffn_only ? 0 : (width + 127) / 128;
   const int attn_splits_max = ffn_only ? 0 : ATTN_MAX_SPLITS;
@@ -289,6 +338,11 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
   const size_t o_perm = take((size_t)R * K * 4);
   h->router_kslices = (H + ROUTER_KSLICE - 1) / ROUTER_KSLICE;
   const size_t o_rpart = take((size_t)h->router_kslices * R * E * 4);
+  const int tc_slots = h->expert_tc ? R * K : 0;
+  const size_t o_ut = take((size_t)(h->expert_tc ? R : 0) * (H / 256) * ACT_TERMS * 128);
+  const size_t o_us = take((size_t)(h->expert_tc ? R : 0) * (H / 256) * ACT_TERMS * 8);
+  const size_t o_tt = take((size_t)tc_slots * (s.moe_inter / 256) * ACT_TERMS * 128);
+  const size_t o_ts = take((size_t)tc_slots * (s.moe_inter / 256) * ACT_TERMS * 8);
   h->arena_bytes = off;
   cudaError_t e = cudaMalloc(&h->arena, h->arena_bytes);
   if (e != cudaSuccess) {
@@ -308,6 +362,12 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
   h->route = reinterpret_cast<RouteInfo*>(h->arena + o_route);
   h->perm = reinterpret_cast<int*>(h->arena + o_perm);
   h->router_part = reinterpret_cast<float*>(h->arena + o_rpart);
+  if (h->expert_tc) {
+    h->u_terms = h->arena + o_ut;
+    h->u_tscales = h->arena + o_us;
+    h->t_terms = h->arena + o_tt;
+    h->t_tscales = h->arena + o_ts;
+  }
 
   // kernel attributes and occupancy
   for (int nt : {1, 2, 4, 6}) {
@@ -329,6 +389,11 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
   if (h->ex_clusters < 1) rc = MONO_ERR_CUDA;
   if (!ffn_only && attention_prepare(s.head_dim) != cudaSuccess) rc = MONO_ERR_CUDA;
   if (router_prepare() != cudaSuccess) rc = MONO_ERR_CUDA;
+  if (h->expert_tc) {
+    int per_sm = 0;
+    if (expert_tc_prepare(&per_sm) != cudaSuccess || per_sm < 1) rc = MONO_ERR_CUDA;
+    h->tc_ctas = h->num_sms * per_sm;
+  }
   if (!rc && (cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
               cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
               cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess))
@@ -521,7 +586,15 @@ int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
   const cudaStream_t stream = run.stream;
   const Launch L{stream, !h->profiling};
   const int R = m.R, H = s.hidden, E = s.n_experts, K = s.topk;
-  TRY(run([&] { return launch_rmsnorm(L, m.seam, R); }));
+  // large steps run the routed experts on the FP4 tensor cores; the seam norm then also
+  // writes u's e2m1 term split
+  const bool tc = h->expert_tc && R * K > EXPERT_SMALL_SLOTS;
+  NormArgs seam = m.seam;
+  if (tc) {
+    seam.terms = h->u_terms;
+    seam.term_scales = h->u_tscales;
+  }
+  TRY(run([&] { return launch_rmsnorm(L, seam, R); }));
   TRY(run([&] {
     return launch_router(L, {h->buf<__half>(MONO_BUF_U), h->w.router, R, E, H, h->router_part});
   }));
@@ -568,18 +641,53 @@ int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
   // every SM at once (items are assigned statically), so they wait for the shared expert.
   const bool late_join = fork && R * K > EXPERT_SMALL_SLOTS;
   if (fork && !late_join) TRY_CUDA(cudaStreamWaitEvent(stream, h->ev_join, 0));
-  TRY(run([&] {
-    return expert_launch(h, R, h->map_ex_gu, h->sc_tma_gu ? &h->map_ex_gu_s : nullptr,
-                         h->w.ex_gu_s, H, 2 * s.moe_inter, s.moe_inter,
-                         s.moe_inter / BOX_ROWS, h->buf<__half>(MONO_BUF_U), H, h->perm,
-                         EPI_SWIGLU_F16, h->buf<void>(MONO_BUF_TR), s.moe_inter, L);
-  }));
-  TRY(run([&] {
-    return expert_launch(h, R, h->map_ex_d, h->sc_tma_d ? &h->map_ex_d_s : nullptr,
-                         h->w.ex_d_s, s.moe_inter, H, 0, H / TILE_M,
-                         h->buf<__half>(MONO_BUF_TR), s.moe_inter, nullptr, EPI_F32,
-                         h->buf<void>(MONO_BUF_YR), H, L);
-  }));
+  if (tc) {
+    ExpertTcParams p = {};
+    p.n_experts = E;
+    p.n_slots = R * K;
+    p.route = h->route;
+    p.clamp = s.swiglu_clamp;
+    p.status = h->status;
+    p.K = H;
+    p.rows_per_mat = 2 * s.moe_inter;
+    p.I = s.moe_inter;
+    p.n_tiles = s.moe_inter / 64;
+    p.act_rows = R;
+    p.rowmap = h->perm;
+    p.item_next = h->route->item_next;
+    p.bterms = h->u_terms;
+    p.bscales = h->u_tscales;
+    p.t16 = h->buf<__half>(MONO_BUF_TR);
+    p.tterms = h->t_terms;
+    p.tscales = h->t_tscales;
+    TRY(run([&] {
+      return launch_expert_tc(L, true, h->map_tc_gu, h->map_tc_gu_s, p, h->tc_ctas);
+    }));
+    p.K = s.moe_inter;
+    p.rows_per_mat = H;
+    p.n_tiles = H / 128;
+    p.rowmap = nullptr;
+    p.item_next = h->route->item_next + 1;
+    p.bterms = h->t_terms;
+    p.bscales = h->t_tscales;
+    p.y = h->buf<float>(MONO_BUF_YR);
+    TRY(run([&] {
+      return launch_expert_tc(L, false, h->map_tc_d, h->map_tc_d_s, p, h->tc_ctas);
+    }));
+  } else {
+    TRY(run([&] {
+      return expert_launch(h, R, h->map_ex_gu, h->sc_tma_gu ? &h->map_ex_gu_s : nullptr,
+                           h->w.ex_gu_s, H, 2 * s.moe_inter, s.moe_inter,
+                           s.moe_inter / BOX_ROWS, h->buf<__half>(MONO_BUF_U), H, h->perm,
+                           EPI_SWIGLU_F16, h->buf<void>(MONO_BUF_TR), s.moe_inter, L);
+    }));
+    TRY(run([&] {
+      return expert_launch(h, R, h->map_ex_d, h->sc_tma_d ? &h->map_ex_d_s : nullptr,
+                           h->w.ex_d_s, s.moe_inter, H, 0, H / TILE_M,
+                           h->buf<__half>(MONO_BUF_TR), s.moe_inter, nullptr, EPI_F32,
+                           h->buf<void>(MONO_BUF_YR), H, L);
+    }));
+  }
   if (late_join) TRY_CUDA(cudaStreamWaitEvent(stream, h->ev_join, 0));
   {
     FinalArgs f = {};

@@ -26,7 +26,8 @@ from tests.parity import layer_metrics, layer_ok, near_tie_rows
 
 pytestmark = pytest.mark.gpu
 
-WORKLOADS = ["tiny", "small_r11", "wide_r9", "full_r1", "full_r24", "full_r48"]
+WORKLOADS = ["tiny", "small_r11", "wide_r9", "mid_r13", "skew_r20", "full_r1", "full_r24",
+             "full_r48"]
 _cache = {}
 
 
