@@ -169,6 +169,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z,
                                             int w, uint64_t* bar) {
   asm volatile(
@@ -433,6 +441,104 @@ __device__ __forceinline__ void split_terms_lane(float v, uint32_t (&words)[ACT_
     w |= __shfl_xor_sync(0xffffffffu, w, 4);
     words[t] = w;
     codes[t] = code;
+  }
+}
+
+}  // namespace mono
+
+namespace mono {
+
+// ------------------------------------------- e4m3 hi/lo split of a many-row activation
+// The dense tensor-core GEMMs (k_dense_tc.cu) take an activation matrix (rows <= 48, K a
+// multiple of 128) as an exact pair hi + lo of e4m3 numbers per element, under one E8M0
+// scale per 32 consecutive K elements of a row (the scale puts the block's largest magnitude
+// in [128, 256); hi = e4m3(v / s), lo = e4m3(v / s - hi), both rounded to nearest even).
+// Every element at least 2^-10 of its block's maximum is reproduced exactly, the smaller ones
+// to within 2^-17 of that maximum.  Its producers write it in the form the GEMM copies into
+// shared memory as is: per 128-element K stage, 128 rows of 128 bytes (row j's hi codes in
+// row j, its lo codes in row SPLIT_LO + j; 16-byte piece c of row n at piece c ^ (n % 8), the
+// 128-byte swizzle), then per stage a 512-byte scale image (MMA column n's four K-block
+// codes at byte (n % 32) * 16 + (n / 32) * 4 + kb).
+constexpr int SPLIT_LO = 64;
+constexpr int SPLIT_STAGE_BYTES = 128 * 128;
+constexpr int SPLIT_IMG_BYTES = 512;
+constexpr int SPLIT_MAX_ROWS = 48;
+
+__device__ __forceinline__ uint32_t e4m3_block_code(float amax) {
+  const int eb = (int)((__float_as_uint(amax) >> 23) & 0xFF);
+  return amax > 0.0f ? (uint32_t)max(eb - 7, 0) : 127u;
+}
+__device__ __forceinline__ float e8m0_inverse(uint32_t code) {
+  return __uint_as_float((254u - code) << 23);
+}
+// v (already divided by the block scale) as hi and lo e4m3 codes.
+__device__ __forceinline__ void e4m3_hilo(float v, uint32_t& hi, uint32_t& lo) {
+  uint32_t h;
+  asm("{\n .reg .b16 t;\n cvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n cvt.u32.u16 %0, t;\n}"
+      : "=r"(h)
+      : "f"(0.0f), "f"(v));
+  uint32_t hf;
+  asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}" : "=r"(hf) : "r"(h));
+  const float hv = __low2float(*reinterpret_cast<const __half2*>(&hf));
+  uint32_t l;
+  asm("{\n .reg .b16 t;\n cvt.rn.satfinite.e4m3x2.f32 t, %1, %2;\n cvt.u32.u16 %0, t;\n}"
+      : "=r"(l)
+      : "f"(0.0f), "f"(v - hv));
+  hi = h & 0xFFu;
+  lo = l & 0xFFu;
+}
+// Byte offset of element k of row n (n = j for hi, SPLIT_LO + j for lo) in the split data.
+__device__ __forceinline__ size_t split_off(int n, int k) {
+  const int w = k & 127;
+  return (size_t)(k >> 7) * SPLIT_STAGE_BYTES + n * 128 + ((((w >> 4) ^ (n & 7))) << 4) + (w & 15);
+}
+// Byte offset of the code of K block k / 32 for MMA column n in the scale images.
+__device__ __forceinline__ size_t split_img_off(int n, int k) {
+  return (size_t)(k >> 7) * SPLIT_IMG_BYTES + (n & 31) * 16 + (n >> 5) * 4 + ((k >> 5) & 3);
+}
+
+// One 32-element block held one element per lane by a whole warp (lane = k % 32): every lane
+// calls it; lanes with !in give 0 and store nothing.
+__device__ __forceinline__ void split_store1(float v, bool in, int row, int k, uint8_t* data,
+                                             uint8_t* img) {
+  const uint32_t code = e4m3_block_code(warp_max(in ? fabsf(v) : 0.0f));
+  uint32_t hi, lo;
+  e4m3_hilo(in ? v * e8m0_inverse(code) : 0.0f, hi, lo);
+  if (in) {
+    data[split_off(row, k)] = (uint8_t)hi;
+    data[split_off(SPLIT_LO + row, k)] = (uint8_t)lo;
+    if ((threadIdx.x & 31) == 0) {
+      img[split_img_off(row, k)] = (uint8_t)code;
+      img[split_img_off(SPLIT_LO + row, k)] = (uint8_t)code;
+    }
+  }
+}
+// A block held eight consecutive elements per lane by an aligned group of four lanes (k8 =
+// the first element, a multiple of 8): every lane of the warp calls it.
+__device__ __forceinline__ void split_store8(const float (&v)[8], bool in, int row, int k8,
+                                             uint8_t* data, uint8_t* img) {
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a = fmaxf(a, in ? fabsf(v[i]) : 0.0f);
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+  const uint32_t code = e4m3_block_code(a);
+  const float inv = e8m0_inverse(code);
+  uint32_t h[2] = {0, 0}, l[2] = {0, 0};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t hb, lb;
+    e4m3_hilo(in ? v[i] * inv : 0.0f, hb, lb);
+    h[i >> 2] |= hb << (8 * (i & 3));
+    l[i >> 2] |= lb << (8 * (i & 3));
+  }
+  if (in) {
+    *reinterpret_cast<uint2*>(data + split_off(row, k8)) = make_uint2(h[0], h[1]);
+    *reinterpret_cast<uint2*>(data + split_off(SPLIT_LO + row, k8)) = make_uint2(l[0], l[1]);
+    if ((k8 & 31) == 0) {
+      img[split_img_off(row, k8)] = (uint8_t)code;
+      img[split_img_off(SPLIT_LO + row, k8)] = (uint8_t)code;
+    }
   }
 }
 

@@ -59,6 +59,26 @@ __device__ __forceinline__ int page_of(const int* table, int max_blocks, int n_r
   return (pb < 0 || pb >= nb) ? -1 : pb;
 }
 
+// Writes this CTA's heads of output row r from a staged f32 copy (values already rounded to
+// bf16): o in f16, and o's e4m3 split (every thread calls it).
+template <int DH>
+__device__ void store_o_staged(const AttnArgs& a, const float* stage, int r, int h0, int hpg) {
+  const int QW = a.n_q * DH, items = hpg * (DH / 8);
+  for (int base = 0; base < items; base += ATTN_THREADS) {
+    const int idx = base + (int)threadIdx.x;
+    const bool in = idx < items;
+    const int h = in ? idx / (DH / 8) : 0, d = in ? 8 * (idx - h * (DH / 8)) : 0;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = in ? stage[h * DH + d + i] : 0.0f;
+    if (in)
+      *reinterpret_cast<uint4*>(a.o + (size_t)r * QW + (h0 + h) * DH + d) =
+          make_uint4(pack_f16x2_sat(v[0], v[1], a.status), pack_f16x2_sat(v[2], v[3], a.status),
+                     pack_f16x2_sat(v[4], v[5], a.status), pack_f16x2_sat(v[6], v[7], a.status));
+    split_store8(v, in, r, (h0 + h) * DH + d, a.e4_data, a.e4_img);
+  }
+}
+
 template <int DH>
 __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(AttnArgs a) {
   using L = AttnSmem<DH>;
@@ -81,9 +101,16 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(AttnArgs a) {
   const int p = a.positions[r];
   if (p < 0) {  // pad row: attention output is zero
     pdl_wait();
-    if (sp == 0)
-      for (int i = tid; i < hpg * DH; i += ATTN_THREADS)
-        a.o[(size_t)r * QW + h0 * DH + i] = __float2half(0.0f);
+    if (sp == 0) {
+      if (a.e4_data) {
+        for (int i = tid; i < hpg * DH; i += ATTN_THREADS) sc[i] = 0.0f;
+        __syncthreads();
+        store_o_staged<DH>(a, sc, r, h0, hpg);
+      } else {
+        for (int i = tid; i < hpg * DH; i += ATTN_THREADS)
+          a.o[(size_t)r * QW + h0 * DH + i] = __float2half(0.0f);
+      }
+    }
     return;
   }
   const int req = a.row_req[r];
@@ -214,8 +241,13 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(AttnArgs a) {
       const float v0 = acc[2 * half] * smax, v1 = acc[2 * half + 1] * smax;
       if (S == 1) {
         const float il = 1.0f / s_l[h];
-        *reinterpret_cast<uint32_t*>(a.o + (size_t)r * QW + (h0 + h) * DH + d) =
-            pack_f16x2_sat(round_bf16(v0 * il), round_bf16(v1 * il), a.status);
+        if (a.e4_data) {  // staged in the scores' memory (free since the softmax)
+          sc[h * DH + d] = round_bf16(v0 * il);
+          sc[h * DH + d + 1] = round_bf16(v1 * il);
+        } else {
+          *reinterpret_cast<uint32_t*>(a.o + (size_t)r * QW + (h0 + h) * DH + d) =
+              pack_f16x2_sat(round_bf16(v0 * il), round_bf16(v1 * il), a.status);
+        }
       } else {
         float* part = a.part + (((size_t)r * a.n_q + h0 + h) * S + sp) * PW;
         *reinterpret_cast<float2*>(part + ATTN_PART_HEAD + d) = make_float2(v0, v1);
@@ -223,7 +255,13 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(AttnArgs a) {
       }
     }
   }
-  if (S == 1) return;
+  if (S == 1) {
+    if (a.e4_data) {
+      __syncthreads();
+      store_o_staged<DH>(a, sc, r, h0, hpg);
+    }
+    return;
+  }
   __threadfence();
   __syncthreads();
   int* ctr = a.counters + r * G + g;
@@ -262,9 +300,20 @@ __global__ void __launch_bounds__(ATTN_THREADS) attn_kernel(AttnArgs a) {
         den = fmaf(f, ls[s], den);
       }
     }
-    *reinterpret_cast<uint2*>(a.o + (size_t)r * QW + (h0 + h) * DH + d) =
-        make_uint2(pack_f16x2_sat(round_bf16(n0 / den), round_bf16(n1 / den), a.status),
-                   pack_f16x2_sat(round_bf16(n2 / den), round_bf16(n3 / den), a.status));
+    if (a.e4_data) {
+      sc[h * DH + d] = round_bf16(n0 / den);
+      sc[h * DH + d + 1] = round_bf16(n1 / den);
+      sc[h * DH + d + 2] = round_bf16(n2 / den);
+      sc[h * DH + d + 3] = round_bf16(n3 / den);
+    } else {
+      *reinterpret_cast<uint2*>(a.o + (size_t)r * QW + (h0 + h) * DH + d) =
+          make_uint2(pack_f16x2_sat(round_bf16(n0 / den), round_bf16(n1 / den), a.status),
+                     pack_f16x2_sat(round_bf16(n2 / den), round_bf16(n3 / den), a.status));
+    }
+  }
+  if (a.e4_data) {
+    __syncthreads();
+    store_o_staged<DH>(a, sc, r, h0, hpg);
   }
   if (tid == 0) *ctr = 0;
 }

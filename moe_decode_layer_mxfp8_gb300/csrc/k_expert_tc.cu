@@ -23,9 +23,12 @@
 #include <algorithm>
 
 #include "kernels.h"
+#include "tc_common.cuh"
 
 namespace mono {
 namespace {
+
+using namespace tc;
 
 constexpr int TC_M = 128;                    // weight rows per tile (the MMA's M)
 constexpr int TC_KC = 256;                   // K elements per stage (128 packed bytes a row)
@@ -54,71 +57,6 @@ constexpr int TMEM_COLS = 256;
 static_assert(SC_COL + 16 * NSTAGE <= TMEM_COLS, "TMEM columns");
 static_assert(TMEM_COLS * TC_CTAS_PER_SM <= 512, "the co-resident CTAs' TMEM fits the SM's");
 constexpr int MAX_GROUPS = MAX_SLOTS;        // row groups at most (<= routed slots)
-
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
-  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-// Descriptor of a scale image (32 rows x 16 B, no swizzle).
-__device__ __forceinline__ uint64_t desc_img(uint32_t saddr) {
-  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) |
-         ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-// Copies a 32-lane x 16-byte image into TMEM columns [taddr, taddr + 4) of every lane
-// quadrant: lane l, column g of the image holds row (or MMA column) l + 32 g's four scale
-// bytes, byte b for K-block b of the 128-element half-stage the image covers.
-__device__ __forceinline__ void tc_cp_img(uint32_t taddr, const void* img) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr),
-               "l"(desc_img(smem_u32(img)))
-               : "memory");
-}
-__device__ __forceinline__ void tc_mma_mxf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                            uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred q;\n setp.ne.b32 q, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], q;\n}"
-      ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
-      : "memory");
-}
-// Arrives on the mbarrier once every MMA / copy this thread has issued so far has completed.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tc_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-// True in one lane of the (converged) warp: the thread that issues the tensor-core work.
-__device__ __forceinline__ bool elect_one() {
-  uint32_t r;
-  asm volatile("{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n selp.u32 %0, 1, 0, e;\n}"
-               : "=r"(r));
-  return r != 0;
-}
-// A bounded wait whose outcome the whole warp shares (every lane calls it).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, int* status,
-                                          volatile int* abort) {
-  return __all_sync(0xffffffffu, pipe_wait(bar, parity, status, abort));
-}
 
 // Items of a launch: hit expert d owns row groups [gpre[d], gpre[d + 1]) (ceil(rows / 16)
 // each) and items [gpre[d] * n_tiles, gpre[d + 1] * n_tiles), tile fastest.

@@ -70,24 +70,21 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(NormArgs a) {
 #pragma unroll
   for (int c = 0; c < NORM_CHUNKS; ++c) {
     const int i = (c * NORM_THREADS + tid) * 8;
-    if (i < a.dim) {
+    const bool in = i < a.dim;
+    float v[8];
+    if (in) {
       float f[8], g[8];
       bf16x8_to_f32(xv[c], f);
       bf16x8_to_f32(gv[c], g);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = round_bf16(f[j] * inv * g[j]);
       uint4 o;
-      o.x = pack_f16x2_sat(round_bf16(f[0] * inv * g[0]), round_bf16(f[1] * inv * g[1]),
-                          a.status);
-      o.y = pack_f16x2_sat(round_bf16(f[2] * inv * g[2]), round_bf16(f[3] * inv * g[3]),
-                          a.status);
-      o.z = pack_f16x2_sat(round_bf16(f[4] * inv * g[4]), round_bf16(f[5] * inv * g[5]),
-                          a.status);
-      o.w = pack_f16x2_sat(round_bf16(f[6] * inv * g[6]), round_bf16(f[7] * inv * g[7]),
-                          a.status);
+      o.x = pack_f16x2_sat(v[0], v[1], a.status);
+      o.y = pack_f16x2_sat(v[2], v[3], a.status);
+      o.z = pack_f16x2_sat(v[4], v[5], a.status);
+      o.w = pack_f16x2_sat(v[6], v[7], a.status);
       *reinterpret_cast<uint4*>(y + i) = o;
       if (a.terms) {  // (a whole warp's chunks are in range or out of it: dim % 256 == 0)
-        float v[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = round_bf16(f[j] * inv * g[j]);
         uint32_t words[ACT_TERMS], codes[ACT_TERMS];
         split_terms_x8(v, words, codes);
         const int q = c * NORM_THREADS + tid;  // 8-element chunk of the row
@@ -100,7 +97,11 @@ __global__ void __launch_bounds__(NORM_THREADS) rmsnorm_kernel(NormArgs a) {
           if ((q & 3) == 0) a.term_scales[(base + t) * 8 + piece] = (uint8_t)codes[t];
         }
       }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
     }
+    if (a.e4_data) split_store8(v, in, r, i, a.e4_data, a.e4_img);  // (every lane)
   }
 }
 
@@ -164,21 +165,25 @@ __global__ void __launch_bounds__(NORM_THREADS) qkv_norm_insert_kernel(QkvNormIn
 #pragma unroll
   for (int c = 0; c < QKV_CHUNKS; ++c) {
     const int i = (c * NORM_THREADS + tid) * 8;
-    if (i < a.q_rank) {
+    const bool in = i < a.q_rank;
+    float v[8];
+    if (in) {
       float f[8], g[8];
       bf16x8_to_f32(qv[c], f);
       bf16x8_to_f32(qg[c], g);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = round_bf16(f[j] * invq * g[j]);
       uint4 o;
-      o.x = pack_f16x2_sat(round_bf16(f[0] * invq * g[0]), round_bf16(f[1] * invq * g[1]),
-                          a.status);
-      o.y = pack_f16x2_sat(round_bf16(f[2] * invq * g[2]), round_bf16(f[3] * invq * g[3]),
-                          a.status);
-      o.z = pack_f16x2_sat(round_bf16(f[4] * invq * g[4]), round_bf16(f[5] * invq * g[5]),
-                          a.status);
-      o.w = pack_f16x2_sat(round_bf16(f[6] * invq * g[6]), round_bf16(f[7] * invq * g[7]),
-                          a.status);
+      o.x = pack_f16x2_sat(v[0], v[1], a.status);
+      o.y = pack_f16x2_sat(v[2], v[3], a.status);
+      o.z = pack_f16x2_sat(v[4], v[5], a.status);
+      o.w = pack_f16x2_sat(v[6], v[7], a.status);
       *reinterpret_cast<uint4*>(a.qlatn + (size_t)r * a.q_rank + i) = o;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
     }
+    if (a.e4_data) split_store8(v, in, r, i, a.e4_data, a.e4_img);  // (every lane)
   }
   float kn[8], g[8];
   bf16x8_to_f32(kg, g);

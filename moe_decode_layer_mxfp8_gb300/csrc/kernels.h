@@ -53,6 +53,10 @@ struct NormArgs {
   // row t mod 8); term_scales [rows][dim / 256][ACT_TERMS][8 blocks]
   uint8_t* terms = nullptr;
   uint8_t* term_scales = nullptr;
+  // optional e4m3 hi/lo split of the normed rows for the dense tensor-core GEMMs (the layout
+  // in common.cuh; rows <= 48)
+  uint8_t* e4_data = nullptr;
+  uint8_t* e4_img = nullptr;
 };
 
 struct QkvNormInsertArgs {
@@ -67,6 +71,8 @@ struct QkvNormInsertArgs {
   uint8_t* cache;
   long long stride_block, stride_tok, num_blocks;
   int* status;
+  uint8_t* e4_data = nullptr;  // optional e4m3 split of qlatn (as NormArgs)
+  uint8_t* e4_img = nullptr;
 };
 
 struct AttnArgs {
@@ -81,6 +87,8 @@ struct AttnArgs {
   float* part;   // [rows, n_q, splits, head_dim + 2]
   int* counters; // [rows, kv_dim / head_dim], left at zero
   int* status;
+  uint8_t* e4_data = nullptr;  // optional e4m3 split of o (as NormArgs)
+  uint8_t* e4_img = nullptr;
 };
 
 constexpr int ROUTER_KSLICE = 1024;  // K per router CTA (the router sums partial logits)
@@ -169,6 +177,35 @@ struct ExpertTcParams {
 cudaError_t expert_tc_prepare(int* ctas_per_sm);
 cudaError_t launch_expert_tc(const Launch&, bool gate_up, const CUtensorMap& wmap,
                              const CUtensorMap& smap, const ExpertTcParams& p, int grid);
+
+// The dense MXFP8 GEMMs of many-row steps on the tensor cores (k_dense_tc.cu).  Weight map:
+// e4m3 [N rows][K bytes], 128-byte swizzle, {128 B, 128 rows} boxes; SwiGLU matrices (gate
+// rows, then the up rows I on) 3D [2][I][K] with {128 B, 64 rows, 2} boxes.  Grid: n_tiles x
+// ksplit CTAs in clusters of ksplit along K (1, 2, 4, 8 or 16; K / (ksplit 128) <= 8 stages).
+// The activations come as their e4m3 split (common.cuh); an F16 or SwiGLU output can be
+// split in turn for the next GEMM.
+struct DenseTcParams {
+  int K, N;
+  int swiglu_I;            // > 0: tile t = gate rows 64t.. and up rows I + 64t..
+  int n_tiles, ksplit;
+  const uint8_t* scales;   // E8M0 [N / 32][K / 32]
+  int scale_ld;            // K / 32
+  const uint8_t* bsplit;   // the activations' split data [K / 128][SPLIT_STAGE_BYTES]
+  const uint8_t* bimg;     // and scale images [K / 128][SPLIT_IMG_BYTES]
+  int rows;                // <= 48
+  int epi;                 // EPI_* as for the MMA-sync GEMM
+  void* out;
+  int out_ld;
+  const __nv_bfloat16* resid;
+  int resid_ld;
+  uint8_t* osplit;         // optional split of the output (EPI_F16, EPI_SWIGLU_F16)
+  uint8_t* oimg;
+  float clamp;
+  int* status;
+};
+cudaError_t dense_tc_prepare();
+int dense_tc_max_clusters(int ksplit);  // co-resident clusters of that size on the GPU
+cudaError_t launch_dense_tc(const Launch&, const CUtensorMap& wmap, const DenseTcParams& p);
 
 // MX GEMM variants: fmt 8 (MXFP8) with nt in {1, 2, 4, 6}; fmt 4 (MXFP4) with nt 1.
 struct GemmVariant {

@@ -31,12 +31,29 @@ const char* const kLaunchNames[kLaunchesPerStep] = {
 
 enum DenseId { D_WQKV = 0, D_WQB, D_WOA, D_WOB, D_SHGU, D_SHD, D_COUNT };
 
+// The e4m3 split of an activation (layout in common.cuh) for the dense tensor-core GEMMs.
+struct SplitBuf {
+  uint8_t* data = nullptr;
+  uint8_t* img = nullptr;
+};
+// The split activations: the inputs of wqkv, wq_b, wo_a, wo_b, the shared gate_up and down
+// (split i feeds dense GEMM i).
+enum SplitId { S_XN = 0, S_QLATN, S_O, S_OA, S_U, S_TS, S_COUNT };
+static_assert((int)S_COUNT == (int)D_COUNT && (int)S_OA == (int)D_WOB && (int)S_TS == (int)D_SHD,
+              "split i is the input of dense GEMM i");
+
 struct DensePlan {
   CUtensorMap map;
   const uint8_t* scales;
   int N, K, n_tiles, ksplit, swiglu_I;
   int max_clusters[7];  // co-resident clusters of size ksplit, by activation-tile count nt
+  // the tensor-core version for many-row steps: its map, tiles and cluster size (0: none)
+  CUtensorMap tc_map;
+  int tc_tiles = 0, tc_ks = 0;
 };
+
+// Steps with more rows than this run the dense GEMMs on the tensor cores.
+constexpr int kDenseTcMinRows = 8;
 
 }  // namespace
 
@@ -70,6 +87,9 @@ struct mono_layer {
   int tc_ctas = 0;  // its grid: co-resident CTAs on every SM
   CUtensorMap map_tc_gu, map_tc_d, map_tc_gu_s, map_tc_d_s;
   uint8_t *u_terms = nullptr, *u_tscales = nullptr, *t_terms = nullptr, *t_tscales = nullptr;
+  // many-row steps: the dense GEMMs on the tensor cores, each fed by its activation's split
+  bool dense_tc[D_COUNT] = {};
+  SplitBuf split[S_COUNT];
   int ctas_gemm8[7] = {};  // by nt
   int ex_ctas = 0;      // persistent CTAs of the expert GEMM (large steps)
   int ex_clusters = 0;  // clusters of EXPERT_CLUSTER CTAs of the K-splitting expert GEMM
@@ -298,6 +318,20 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
       delete h;
       return MONO_ERR_CUDA;
     }
+    // tensor-core map: {128 B, 128 rows} boxes, SwiGLU matrices as [2][I][K] with 64-row boxes
+    bool tc_ok;
+    if (d.swiglu_I) {
+      const long long dims[3] = {d.K, d.swiglu_I, 2}, st[2] = {d.K, (long long)d.swiglu_I * d.K};
+      const int box[3] = {128, 64, 2};
+      tc_ok = d.swiglu_I % 64 == 0 && make_map_nd(&d.tc_map, defs[i].w, 3, dims, st, box, true);
+      d.tc_tiles = d.swiglu_I / 64;
+    } else {
+      const long long dims[2] = {d.K, d.N}, st[1] = {d.K};
+      const int box[2] = {128, 128};
+      tc_ok = make_map_nd(&d.tc_map, defs[i].w, 2, dims, st, box, true);
+      d.tc_tiles = (d.N + 127) / 128;
+    }
+    d.tc_ks = tc_ok ? -1 : 0;  // K split chosen once the kernel's occupancy is known
   }
   if (!make_map(&h->map_ex_gu, wt->ex_gu, (long long)E * 2 * s.moe_inter, H / 2) ||
       !make_map(&h->map_ex_d, wt->ex_d, (long long)E * H, s.moe_inter / 2)) {
@@ -338,6 +372,15 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
   const size_t o_perm = take((size_t)R * K * 4);
   h->router_kslices = (H + ROUTER_KSLICE - 1) / ROUTER_KSLICE;
   const size_t o_rpart = take((size_t)h->router_kslices * R * E * 4);
+  // the activation splits of many-row steps (used by the GEMMs that get a tensor-core plan)
+  const bool many_rows = R > kDenseTcMinRows;
+  const int split_k[S_COUNT] = {ffn_only ? 0 : H, q_rank, QW, o_rank, H, s.shared_inter};
+  size_t o_split[S_COUNT][2];
+  for (int i = 0; i < S_COUNT; ++i) {
+    const size_t stages = many_rows ? (size_t)split_k[i] / 128 : 0;
+    o_split[i][0] = take(stages * SPLIT_STAGE_BYTES);
+    o_split[i][1] = take(stages * SPLIT_IMG_BYTES);
+  }
   const int tc_slots = h->expert_tc ? R * K : 0;
   const size_t o_ut = take((size_t)(h->expert_tc ? R : 0) * (H / 256) * ACT_TERMS * 128);
   const size_t o_us = take((size_t)(h->expert_tc ? R : 0) * (H / 256) * ACT_TERMS * 8);
@@ -362,6 +405,12 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
   h->route = reinterpret_cast<RouteInfo*>(h->arena + o_route);
   h->perm = reinterpret_cast<int*>(h->arena + o_perm);
   h->router_part = reinterpret_cast<float*>(h->arena + o_rpart);
+  if (many_rows)
+    for (int i = 0; i < S_COUNT; ++i)
+      if (split_k[i] > 0) {
+        h->split[i].data = h->arena + o_split[i][0];
+        h->split[i].img = h->arena + o_split[i][1];
+      }
   if (h->expert_tc) {
     h->u_terms = h->arena + o_ut;
     h->u_tscales = h->arena + o_us;
@@ -389,6 +438,32 @@ int mono_layer_build(const mono_layer_spec* spec, const mono_layer_weights* wt, 
   if (h->ex_clusters < 1) rc = MONO_ERR_CUDA;
   if (!ffn_only && attention_prepare(s.head_dim) != cudaSuccess) rc = MONO_ERR_CUDA;
   if (router_prepare() != cudaSuccess) rc = MONO_ERR_CUDA;
+  if (dense_tc_prepare() != cudaSuccess) rc = MONO_ERR_CUDA;
+  for (int i = ffn_only ? D_SHGU : 0; i < D_COUNT && !rc && many_rows; ++i) {
+    // K split: the largest power of two up to 16 that keeps one CTA per SM, whole stages
+    // (at most 8 a CTA), every cluster of the launch resident at once and an owner's receive
+    // slots within its rings; else the plain GEMM
+    DensePlan& d = h->dense[i];
+    if (!d.tc_ks) continue;
+    d.tc_ks = 0;
+    int ks = 1;
+    while (d.tc_tiles * ks * 2 <= h->num_sms && (d.K / 128) % (ks * 2) == 0 && ks * 2 <= 16)
+      ks *= 2;
+    const int nb = d.swiglu_I ? 2 : 4, brows = d.swiglu_I ? 64 : 32;
+    for (; ks >= 1; ks /= 2) {
+      const bool fits = d.K / (ks * 128) <= 8 &&
+                        (ks == 1 || (nb + ks - 1) / ks * ks * brows * 49 * 4 <= 128 * 1024);
+      if (fits && (ks == 1 || dense_tc_max_clusters(ks) >= d.tc_tiles)) {
+        d.tc_ks = ks;
+        break;
+      }
+    }
+  }
+  // a GEMM whose input is another GEMM's output needs that one on the tensor cores too (its
+  // epilogue writes the split)
+  for (int i = 0; i < D_COUNT; ++i) h->dense_tc[i] = many_rows && h->dense[i].tc_ks > 0;
+  h->dense_tc[D_WOB] = h->dense_tc[D_WOB] && h->dense_tc[D_WOA];
+  h->dense_tc[D_SHD] = h->dense_tc[D_SHD] && h->dense_tc[D_SHGU];
   if (h->expert_tc) {
     int per_sm = 0;
     if (expert_tc_prepare(&per_sm) != cudaSuccess || per_sm < 1) rc = MONO_ERR_CUDA;
@@ -504,10 +579,43 @@ struct Enqueue {
   } while (0)
 
 // One MXFP8 dense GEMV of the layer over R rows.
+// Dense GEMM id runs on the tensor cores in this step, fed by split id (which its producer
+// then writes).
+bool use_dense_tc(const mono_layer* h, int R, int id) {
+  return h->dense_tc[id] && R > kDenseTcMinRows;
+}
+const SplitBuf* split_of(const mono_layer* h, int R, int id) {
+  return use_dense_tc(h, R, id) ? &h->split[id] : nullptr;
+}
+
 cudaError_t dense_launch(const mono_layer* h, int id, int R, const __half* act, int act_ld,
                          int epi, void* outp, int out_ld, const __nv_bfloat16* resid,
-                         const Launch& L) {
+                         const Launch& L, const SplitBuf* in = nullptr,
+                         const SplitBuf* out = nullptr) {
   const DensePlan& d = h->dense[id];
+  if (in && use_dense_tc(h, R, id)) {
+    DenseTcParams q = {};
+    q.K = d.K;
+    q.N = d.N;
+    q.swiglu_I = d.swiglu_I;
+    q.n_tiles = d.tc_tiles;
+    q.ksplit = d.tc_ks;
+    q.scales = d.scales;
+    q.scale_ld = d.K / 32;
+    q.bsplit = in->data;
+    q.bimg = in->img;
+    q.rows = R;
+    q.osplit = out ? out->data : nullptr;
+    q.oimg = out ? out->img : nullptr;
+    q.epi = epi;
+    q.out = outp;
+    q.out_ld = out_ld;
+    q.resid = resid;
+    q.resid_ld = h->spec.hidden;
+    q.clamp = h->spec.swiglu_clamp;
+    q.status = h->status;
+    return launch_dense_tc(L, d.tc_map, q);
+  }
   const int nt = nt_bucket(R);
   GemmParams p = {};
   p.scales = d.scales;
@@ -594,18 +702,19 @@ int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
     seam.terms = h->u_terms;
     seam.term_scales = h->u_tscales;
   }
+  if (const SplitBuf* sp = split_of(h, R, S_U)) seam.e4_data = sp->data, seam.e4_img = sp->img;
   TRY(run([&] { return launch_rmsnorm(L, seam, R); }));
-  TRY(run([&] {
-    return launch_router(L, {h->buf<__half>(MONO_BUF_U), h->w.router, R, E, H, h->router_part});
-  }));
-  // The shared expert depends only on u: it runs on the side stream, forked after the router,
-  // so that it overlaps the top-k and, in large steps, the routed experts.  The top-k is
-  // launched first: its one CTA then takes an SM (it asks for most of one, so that no GEMM CTA
-  // shares it) before the shared expert's GEMM CTAs fill the GPU.  While profiling,
-  // everything stays on one stream in launch-name order.
+  // The shared expert depends only on u: it runs on the side stream, forked right after the
+  // seam norm, so that it overlaps the router and the top-k and is done (or nearly) before
+  // the routed experts' persistent CTAs take every SM -- forked later, its down GEMM found no
+  // SM free until the routed gate_up drained and then held up the routed down.  While
+  // profiling, everything stays on one stream in launch-name order.
   const bool fork = !h->profiling;
   const Launch Ls{fork ? h->side : stream, !h->profiling};
   if (fork) TRY_CUDA(cudaEventRecord(h->ev_fork, stream));
+  TRY(run([&] {
+    return launch_router(L, {h->buf<__half>(MONO_BUF_U), h->w.router, R, E, H, h->router_part});
+  }));
   {
     TopkArgs t = {};
     t.partial = h->router_part;
@@ -629,11 +738,12 @@ int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
   if (fork) TRY_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
   TRY(run([&] {
     return dense_launch(h, D_SHGU, R, h->buf<__half>(MONO_BUF_U), H, EPI_SWIGLU_F16,
-                        h->buf<void>(MONO_BUF_TS), s.shared_inter, nullptr, Ls);
+                        h->buf<void>(MONO_BUF_TS), s.shared_inter, nullptr, Ls,
+                        split_of(h, R, S_U), split_of(h, R, S_TS));
   }));
   TRY(run([&] {
     return dense_launch(h, D_SHD, R, h->buf<__half>(MONO_BUF_TS), s.shared_inter, EPI_F32,
-                        h->buf<void>(MONO_BUF_YS), H, nullptr, Ls);
+                        h->buf<void>(MONO_BUF_YS), H, nullptr, Ls, split_of(h, R, S_TS));
   }));
   if (fork) TRY_CUDA(cudaEventRecord(h->ev_join, h->side));
   // Large steps: the persistent expert GEMM starts right after the top-k and the shared
@@ -741,11 +851,12 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     NormArgs n = {x, H, (const __nv_bfloat16*)h->w.attn_norm, H, s.eps,
                   h->buf<__half>(MONO_BUF_XN), H};
     n.status = h->status;
+    if (const SplitBuf* sp = split_of(h, R, S_XN)) n.e4_data = sp->data, n.e4_img = sp->img;
     return launch_rmsnorm(L, n, R);
   }));
   TRY(run([&] {
     return dense_launch(h, D_WQKV, R, h->buf<__half>(MONO_BUF_XN), H, EPI_BF16,
-                        h->buf<void>(MONO_BUF_QKV), A, nullptr, L);
+                        h->buf<void>(MONO_BUF_QKV), A, nullptr, L, split_of(h, R, S_XN));
   }));
   {
     QkvNormInsertArgs q = {};
@@ -768,11 +879,12 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     q.stride_tok = a->kv_stride_tok;
     q.num_blocks = a->kv_num_blocks;
     q.status = h->status;
+    if (const SplitBuf* sp = split_of(h, R, S_QLATN)) q.e4_data = sp->data, q.e4_img = sp->img;
     TRY(run([&] { return launch_qkv_norm_insert(L, q, R); }));
   }
   TRY(run([&] {
     return dense_launch(h, D_WQB, R, h->buf<__half>(MONO_BUF_QLATN), s.q_rank, EPI_BF16,
-                        h->buf<void>(MONO_BUF_Q), QW, nullptr, L);
+                        h->buf<void>(MONO_BUF_Q), QW, nullptr, L, split_of(h, R, S_QLATN));
   }));
 
   // ---------------------------------------------------------------- K2: attention back
@@ -802,15 +914,17 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
     t.part = h->attn_part;
     t.counters = h->attn_counters;
     t.status = h->status;
+    if (const SplitBuf* sp = split_of(h, R, S_O)) t.e4_data = sp->data, t.e4_img = sp->img;
     TRY(run([&] { return launch_attention(L, t, s.head_dim, G); }));
   }
   TRY(run([&] {
     return dense_launch(h, D_WOA, R, h->buf<__half>(MONO_BUF_O), QW, EPI_F16,
-                        h->buf<void>(MONO_BUF_OA), s.o_rank, nullptr, L);
+                        h->buf<void>(MONO_BUF_OA), s.o_rank, nullptr, L, split_of(h, R, S_O),
+                        split_of(h, R, S_OA));
   }));
   TRY(run([&] {
     return dense_launch(h, D_WOB, R, h->buf<__half>(MONO_BUF_OA), s.o_rank, EPI_RESID_BF16,
-                        h->buf<void>(MONO_BUF_H), H, x, L);
+                        h->buf<void>(MONO_BUF_H), H, x, L, split_of(h, R, S_OA));
   }));
 
   // ---------------------------------------------------------------- K2: FFN seam and MoE
