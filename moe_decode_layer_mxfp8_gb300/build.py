@@ -18,7 +18,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmono_layer.so")
-SOURCES = ["k_gemm.cu", "k_expert_tc.cu", "k_norm.cu", "k_attn.cu", "k_route.cu", "mono_layer.cu",
+SOURCES = ["k_gemm.cu", "k_expert_tc.cu", "k_dense_tc.cu", "k_norm.cu", "k_attn.cu", "k_route.cu", "mono_layer.cu",
            "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
