@@ -634,12 +634,12 @@ def _workload_desc(name, spec, rows):
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the dominant
-# kernel, from an ncu capture of one launch, keyed by the md5 of the GEMM sources it was
+# kernel, from an ncu capture of one launch, keyed by the md5 of the kernel's sources it was
 # taken on: reported only while those are unchanged.
 NCU_TRAFFIC = {
-    ("full_r48", "expert_gate_up"): (499_593_216, "6fe50f48436f2a0ffda5000e987420f8"
-                                                  "11ea0d6a1dd3a6dc5a7280a56fec6f62"
-                                                  "f4a1d65a57a56dec41dc2f07972e1b1a"),
+    ("full_r48", "expert_gate_up"): (503_954_176, "79b5b3db54dd073cb417281c19334a8e"
+                                                  "06e4e11ed408713cfcd80ad3695d0c0c"
+                                                  "e1e9f56c5c27e1e05610593a630892b8"),
 }
 
 
@@ -647,7 +647,7 @@ def _gemm_source_hash():
     import hashlib
     d = os.path.join(os.path.dirname(os.path.abspath(__file__)), "moe_decode_layer_mxfp8_gb300", "csrc")
     return "".join(hashlib.md5(open(os.path.join(d, f), "rb").read()).hexdigest()
-                   for f in ("mx_gemm.cuh", "k_gemm.cu", "common.cuh"))
+                   for f in ("k_expert_tc.cu", "tc_common.cuh", "common.cuh"))
 
 
 def run_eager(name, n):

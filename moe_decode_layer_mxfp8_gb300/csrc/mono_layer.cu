@@ -746,11 +746,10 @@ int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
                         h->buf<void>(MONO_BUF_YS), H, nullptr, Ls, split_of(h, R, S_TS));
   }));
   if (fork) TRY_CUDA(cudaEventRecord(h->ev_join, h->side));
-  // Large steps: the persistent expert GEMM starts right after the top-k and the shared
-  // expert joins before the final combine.  Small steps: the routed experts' clusters want
-  // every SM at once (items are assigned statically), so they wait for the shared expert.
-  const bool late_join = fork && R * K > EXPERT_SMALL_SLOTS;
-  if (fork && !late_join) TRY_CUDA(cudaStreamWaitEvent(stream, h->ev_join, 0));
+  // The routed experts start right after the top-k and the shared expert joins before the
+  // final combine.  (Small steps' routed clusters take their items statically; those placed
+  // on SMs the shared expert still holds start a little later, which costs less than
+  // waiting for the whole shared expert: 1 row 81.3 -> 75.0 us, 6 draft rows 82.5 -> 77.6.)
   if (tc) {
     ExpertTcParams p = {};
     p.n_experts = E;
@@ -798,7 +797,7 @@ int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
                            h->buf<void>(MONO_BUF_YR), H, L);
     }));
   }
-  if (late_join) TRY_CUDA(cudaStreamWaitEvent(stream, h->ev_join, 0));
+  if (fork) TRY_CUDA(cudaStreamWaitEvent(stream, h->ev_join, 0));
   {
     FinalArgs f = {};
     f.x = m.x;
