@@ -282,9 +282,12 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t e) {
 // v = sum_t c_t * 2^(s_t - 127).  Term t's scale is the smallest power of two that brings
 // the block's remaining residual within +-6 (the largest e2m1 magnitude), the codes round
 // the residual to nearest (even), and the residual left after a term is exact in f32: every
-// value is a bf16 number and each term removes a leading part of its bits.  Eight terms
-// leave nothing of the layer's activations (each term shrinks a block's largest residual at
-// least threefold, usually far more); the products then equal those of the f16 path.
+// value is a bf16 number and each term removes a leading part of its bits.  Each term
+// shrinks the block's largest residual at least threefold (the residual's magnitude a lies in
+// (3s, 6s] and rounding leaves at most s), so eight leave less than 3^-8 of the block's
+// largest magnitude; a bf16 value has 8 significant bits, and blocks of normal or
+// heavy-tailed data come out exact (in a CPU simulation, 0 of 640,000 elements off; with
+// log-normal magnitudes spread over e^+-4, 0.04 % off by at most 2.5e-8 of the block max).
 constexpr int ACT_TERMS = 8;
 
 // Two f32 values rounded to nearest-even e2m1 (saturating at +-6) in one byte, lo in the low
