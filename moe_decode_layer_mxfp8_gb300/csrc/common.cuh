@@ -341,6 +341,11 @@ __device__ __forceinline__ float warp_max(float v) {
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
+// The largest of the warp's magnitudes (a >= 0, not NaN) in one reduction: non-negative
+// floats order as their bit patterns.
+__device__ __forceinline__ float warp_max_abs(float a) {
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(a)));
+}
 
 // Block-wide sum / max; `red` is a 32-float shared buffer; every thread gets the result.
 __device__ __forceinline__ float block_sum(float v, float* red) {
@@ -433,7 +438,7 @@ __device__ __forceinline__ void split_terms_lane(float v, uint32_t (&words)[ACT_
   float r = v;
 #pragma unroll
   for (int t = 0; t < ACT_TERMS; ++t) {
-    const uint32_t code = e2m1_term_code(warp_max(fabsf(r)));
+    const uint32_t code = e2m1_term_code(warp_max_abs(fabsf(r)));
     const uint32_t nib = e2m1x2_of(r * e8m0_inv_pow2(code), 0.0f) & 0xFu;
     uint32_t h[4];
     e2m1x8_to_f16x8(nib, h);
@@ -504,7 +509,7 @@ __device__ __forceinline__ size_t split_img_off(int n, int k) {
 // calls it; lanes with !in give 0 and store nothing.
 __device__ __forceinline__ void split_store1(float v, bool in, int row, int k, uint8_t* data,
                                              uint8_t* img) {
-  const uint32_t code = e4m3_block_code(warp_max(in ? fabsf(v) : 0.0f));
+  const uint32_t code = e4m3_block_code(warp_max_abs(in ? fabsf(v) : 0.0f));
   uint32_t hi, lo;
   e4m3_hilo(in ? v * e8m0_inverse(code) : 0.0f, hi, lo);
   if (in) {

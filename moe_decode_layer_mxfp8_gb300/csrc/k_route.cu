@@ -157,7 +157,7 @@ __device__ __noinline__ Pick select_topk(const float* z, int E, int k, int lpr, 
 }
 
 constexpr int TOPK_THREADS = 512;
-constexpr int TOPK_BATCH = 4;  // logits per thread in flight at once
+constexpr int TOPK_BATCH = 12;  // logits per thread in flight at once (48 rows x 128 experts)
 template <int KSL>  // K slices of the router partials at most
 __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
   extern __shared__ float s_z[];  // [rows][E] logits
