@@ -650,6 +650,26 @@ def _gemm_source_hash():
                    for f in ("k_expert_tc.cu", "tc_common.cuh", "common.cuh"))
 
 
+def schedule_probe():
+    """The cost of one stage boundary of a layer step, both ways (csrc/probe_schedule.cu): a
+    graph of n programmatically serialised launches of a kernel that only triggers and waits,
+    against n grid-wide barriers inside one cooperative launch of one CTA per SM."""
+    import ctypes as C
+    from moe_decode_layer_mxfp8_gb300 import build
+    lib = C.CDLL(build.build_probe())
+    torch.cuda.init()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    out = dict(sms=sms, pdl_boundary_us={}, grid_barrier_us={})
+    v = C.c_float(0.0)
+    for ctas in (1, 48, sms, 2 * sms):  # the step's launch widths: 1 (top-k) .. 2 x SMs
+        rc = lib.mono_probe_pdl_chain(64, ctas, 50, C.byref(v))
+        out["pdl_boundary_us"][str(ctas)] = round(v.value, 3) if rc == 0 else f"error {rc}"
+    for ctas in (sms // 2, sms):
+        rc = lib.mono_probe_grid_barrier(2000, ctas, C.byref(v))
+        out["grid_barrier_us"][str(ctas)] = round(v.value, 3) if rc == 0 else f"error {rc}"
+    print(json.dumps(out))
+
+
 def run_eager(name, n):
     """N eager layer steps (launch order: per step 15 launches, see mono_layer_launch_name)."""
     from moe_decode_layer_mxfp8_gb300 import build
@@ -683,10 +703,16 @@ def main():
     ap.add_argument("--eager", type=int, default=0, metavar="N",
                     help="only run N eager steps of the workload (one layer copy) and exit: a "
                          "short command for ncu captures of single launches")
+    ap.add_argument("--schedule-probe", action="store_true",
+                    help="only measure a stage boundary as a programmatically serialised launch "
+                         "and as a grid-wide barrier of one persistent launch, and exit")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.eager:
         run_eager(args.workload, args.eager)
+        return
+    if args.schedule_probe:
+        schedule_probe()
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -85,5 +85,22 @@ def build(force: bool = False, verbose_ptxas: bool = False, quiet: bool = True) 
     return LIB
 
 
+PROBE_LIB = os.path.join(HERE, "libmono_probe.so")
+
+
+def build_probe(force: bool = False) -> str:
+    """The schedule probe (csrc/probe_schedule.cu), its own small library."""
+    src = os.path.join(CSRC, "probe_schedule.cu")
+    if force or not os.path.exists(PROBE_LIB) or os.path.getmtime(src) > os.path.getmtime(PROBE_LIB):
+        tmp = PROBE_LIB + f".tmp{os.getpid()}"
+        cmd = [_nvcc()] + ARCH + ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
+                                  "-cudart", "static", src, "-o", tmp]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed on probe_schedule.cu:\n" + r.stderr)
+        os.replace(tmp, PROBE_LIB)
+    return PROBE_LIB
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, quiet=False))
