@@ -84,10 +84,102 @@ __device__ __forceinline__ TcItem tc_item(const TcRoute& rt, int n_tiles, int q)
   return it;
 }
 
+// ---------------------------------------------------------------- shared-expert down items
+// The down launch also runs the shared expert's down GEMM (MXFP8, e4m3 weights with 32 x 32
+// E8M0 scales): items (128-row tile of H, a half of at most SH_ROWS activation rows), ahead
+// of the routed items.  Their MMAs are kind::mxf8f6f4 (scale_vec::1X); the activations are
+// t_s's e4m3 hi/lo split as the shared gate_up wrote it (common.cuh), a stage's B tile being
+// the half's hi rows at rows [0, SH_ROWS) and its lo rows at [SH_ROWS, 2 SH_ROWS).
+constexpr int SH_ROWS = 24;
+static_assert(2 * SH_ROWS <= TC_NMAX && 2 * SH_ROWS * TERM_ROW <= B_BYTES, "a half's B tile");
+static_assert(SPLIT_IMG_BYTES <= SB_BYTES && 4 * 16 <= SA_BYTES, "a half's scales");
+
+struct ShItem {
+  int tile, i0, nh;  // output tile, first activation row, rows (1 .. SH_ROWS)
+};
+__device__ __forceinline__ ShItem sh_item(const ExpertTcParams& p, int q) {
+  ShItem it;
+  it.tile = q / p.sh_halves;
+  it.i0 = (q - it.tile * p.sh_halves) * SH_ROWS;
+  it.nh = min(SH_ROWS, p.sh_rows - it.i0);
+  return it;
+}
+// Producer: one stage of a shared item (elected lane).
+__device__ __forceinline__ void sh_issue(const ExpertTcParams& p, const CUtensorMap* shmap,
+                                         const ShItem& it, int c, uint8_t* st, uint64_t* full) {
+  mbar_arrive_expect_tx(full, A_BYTES + 2 * it.nh * TERM_ROW + SPLIT_IMG_BYTES + 4 * 16);
+  tma_load_2d(st + A_OFF, shmap, c * 128, it.tile * TC_M, full);
+  // the tile's four 32-row scale blocks: the 16-byte runs holding this stage's 4 K blocks
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+    bulk_load_g2s(st + SA_OFF + 16 * g,
+                  p.sh_scales + (size_t)(it.tile * 4 + g) * p.sh_scale_ld + ((c * 4) & ~15), 16,
+                  full);
+  const uint8_t* src = p.sh_bsplit + (size_t)c * SPLIT_STAGE_BYTES;
+  bulk_load_g2s(st + B_OFF, src + it.i0 * TERM_ROW, it.nh * TERM_ROW, full);
+  bulk_load_g2s(st + B_OFF + SH_ROWS * TERM_ROW, src + (SPLIT_LO + it.i0) * TERM_ROW,
+                it.nh * TERM_ROW, full);
+  bulk_load_g2s(st + SB_OFF, p.sh_bimg + (size_t)c * SPLIT_IMG_BYTES, SPLIT_IMG_BYTES, full);
+}
+// MMA warp: one stage of a shared item -- the scale images (every lane), then the copies and
+// MMAs (the elected lane).  A image: the tile's row block g's 4 scale bytes in column g of
+// every lane; B image: MMA column n (hi row i0 + n, or lo row i0 + n - SH_ROWS) at lane n % 32,
+// column n / 32, taken from the split's image (hi column j's word).
+__device__ __forceinline__ void sh_mma(const ExpertTcParams& p, const ShItem& it, int c,
+                                       uint8_t* st, uint32_t d0, uint32_t sc, int lane,
+                                       bool first) {
+  uint32_t wa[4], wb[4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    wa[g] = *reinterpret_cast<const uint32_t*>(st + SA_OFF + 16 * g + ((c * 4) & 15));
+    const int n = lane + 32 * g;
+    const int j = it.i0 + (n < SH_ROWS ? n : n - SH_ROWS);
+    wb[g] = n < 2 * SH_ROWS && j < p.sh_rows
+                ? *reinterpret_cast<const uint32_t*>(st + SB_OFF + (j & 31) * 16 + (j >> 5) * 4)
+                : 0x7F7F7F7Fu;
+  }
+  *reinterpret_cast<uint4*>(st + IMG_OFF + lane * 16) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+  *reinterpret_cast<uint4*>(st + IMG_OFF + 2 * IMG + lane * 16) =
+      make_uint4(wb[0], wb[1], wb[2], wb[3]);
+  fence_proxy_async_shared();
+  __syncwarp();
+  const uint32_t a0 = smem_u32(st + A_OFF), b0 = smem_u32(st + B_OFF);
+  // kind::mxf8f6f4, A and B e4m3, E8M0 scales, M = 128, N = 2 SH_ROWS
+  const uint32_t idesc = (1u << 23) | ((uint32_t)((2 * SH_ROWS) >> 3) << 17) |
+                         ((uint32_t)(TC_M >> 4) << 24);
+  if (elect_one()) {
+    tc_fence_after();
+    tc_cp_img(sc, st + IMG_OFF);
+    tc_cp_img(sc + 8, st + IMG_OFF + 2 * IMG);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)  // K = 32 each; scale byte k of the stage's words
+      tc_mma_mxf8(d0, desc_sw128(a0 + 32 * k), desc_sw128(b0 + 32 * k),
+                  idesc | ((uint32_t)k << 4) | ((uint32_t)k << 29), sc, sc + 8,
+                  (!first || k > 0) ? 1u : 0u);
+  }
+}
+// Epilogue warp (TMEM lane quadrant quad) of a shared item: y_s rows i0 .. i0 + nh of its 32
+// output columns, each the sum of the hi and lo accumulator columns.
+__device__ __forceinline__ void sh_epilogue(const ExpertTcParams& p, const ShItem& it,
+                                            uint32_t taddr, int quad, int lane) {
+  uint32_t r0[32], r1[32];
+  tc_ld32(taddr, r0);
+  tc_ld32(taddr + 32, r1);
+  tc_wait_ld();
+  const int col = it.tile * TC_M + quad * 32 + lane;
+#pragma unroll
+  for (int j = 0; j < SH_ROWS; ++j) {
+    const int n = SH_ROWS + j;
+    const float v = __uint_as_float(r0[j]) + __uint_as_float(n < 32 ? r0[n & 31] : r1[n & 31]);
+    if (j < it.nh) p.ys[(size_t)(it.i0 + j) * p.rows_per_mat + col] = v;
+  }
+}
+
 template <bool GU>
 __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM)
     expert_tc_kernel(const __grid_constant__ CUtensorMap wmap,
-                     const __grid_constant__ CUtensorMap smap, const ExpertTcParams p) {
+                     const __grid_constant__ CUtensorMap smap,
+                     const __grid_constant__ CUtensorMap shmap, const ExpertTcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -197,7 +289,10 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM)
   for (int d = tid; d < n_hit; d += TC_THREADS)
     for (int g = rt.gpre[d]; g < rt.gpre[d + 1] && g < MAX_GROUPS; ++g) rt.gexp[g] = (uint8_t)d;
   __syncthreads();
-  const int n_items = min(rt.gpre[n_hit], MAX_GROUPS) * p.n_tiles;
+  // the shared expert's down items come first (each streams p.sh_nck stages, more than a
+  // routed item's), then the routed items
+  const int n_sh = GU ? 0 : p.sh_tiles * p.sh_halves;
+  const int n_items = n_sh + min(rt.gpre[n_hit], MAX_GROUPS) * p.n_tiles;
 
   if (warp == 0) {
     // ---------------------------------------------------------------------------- producer
@@ -208,7 +303,22 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM)
     while (q < n_items) {
       int qn = 0;
       if (lane == 0) qn = atomicAdd(p.item_next, 1);
-      const TcItem it = tc_item(rt, p.n_tiles, q);
+      if (!GU && q < n_sh) {
+        const ShItem si = sh_item(p, q);
+        for (int c = 0; c < p.sh_nck; ++c, ++iter) {
+          const int s = iter % NSTAGE;
+          if (!warp_wait(&empty[s], ((iter / NSTAGE) & 1) ^ 1, p.status, abort))
+            goto producer_done;
+          if (elect_one()) {
+            if (c == 0) slot_q[s] = q;  // published by the arrival in sh_issue
+            sh_issue(p, &shmap, si, c, smem + s * STAGE, &full[s]);
+          }
+          __syncwarp();
+        }
+        q = __shfl_sync(0xffffffffu, qn, 0);
+        continue;
+      }
+      const TcItem it = tc_item(rt, p.n_tiles, q - n_sh);
       int arow = 0;
       if (GU && lane < it.n) arow = rt.rowmap[it.slot0 + lane];
       const uint32_t tx = A_BYTES + SA_BYTES + it.n * (ACT_TERMS * TERM_ROW + TERM_SC);
@@ -273,9 +383,26 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM)
         if (elect_one()) tc_commit(&tfull[b]);  // (the issuing thread's commits)
         break;
       }
-      const TcItem it = tc_item(rt, p.n_tiles, q);
-      const int ncol = (it.n * ACT_TERMS + 15) & ~15;
       const uint32_t d0 = tmem + b * TC_NMAX;
+      if (!GU && q < n_sh) {
+        const ShItem si = sh_item(p, q);
+        bool sok = true;
+        for (int c = 0; c < p.sh_nck; ++c, ++iter) {
+          s = iter % NSTAGE;
+          if (c > 0 && !warp_wait(&full[s], (iter / NSTAGE) & 1, p.status, abort)) {
+            sok = false;
+            break;
+          }
+          sh_mma(p, si, c, smem + s * STAGE, d0, tmem + SC_COL + s * 16, lane, c == 0);
+          if (elect_one()) tc_commit(&empty[s]);
+          __syncwarp();
+        }
+        if (!sok) break;
+        if (elect_one()) tc_commit(&tfull[b]);
+        continue;
+      }
+      const TcItem it = tc_item(rt, p.n_tiles, q - n_sh);
+      const int ncol = (it.n * ACT_TERMS + 15) & ~15;
       const uint32_t idesc_base = (1u << 7) | (1u << 10) | ((uint32_t)(ncol >> 3) << 17) |
                                   (1u << 23) | ((uint32_t)(TC_M >> 4) << 24);
       bool ok = true;
@@ -357,7 +484,15 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM)
       tc_fence_after();
       const int q = acc_q[b];
       if (q < 0) break;
-      const TcItem it = tc_item(rt, p.n_tiles, q);
+      if (!GU && q < n_sh) {
+        sh_epilogue(p, sh_item(p, q), tmem + ((uint32_t)(quad * 32) << 16) + b * TC_NMAX, quad,
+                    lane);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[b]);
+        continue;
+      }
+      const TcItem it = tc_item(rt, p.n_tiles, q - n_sh);
       // this lane's weight row's value for each routed row: the sum of its eight term columns
       float y[TC_ROWS];
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + b * TC_NMAX;
@@ -470,15 +605,21 @@ cudaError_t expert_tc_prepare(int* ctas_per_sm) {
 }
 
 cudaError_t launch_expert_tc(const Launch& L, bool gate_up, const CUtensorMap& wmap,
-                             const CUtensorMap& smap, const ExpertTcParams& p, int grid) {
+                             const CUtensorMap& smap, const CUtensorMap& shmap,
+                             const ExpertTcParams& p, int grid) {
   if (p.K % TC_KC || (gate_up && (p.I % 64 || p.I % TC_KC)) || (!gate_up && p.rows_per_mat % TC_M) ||
       !p.item_next || !p.route || p.n_slots > MAX_SLOTS)
     return cudaErrorInvalidValue;
+  if (!gate_up && p.sh_tiles > 0 &&
+      (p.sh_rows < 1 || p.sh_halves != (p.sh_rows + SH_ROWS - 1) / SH_ROWS || p.sh_nck < 1 ||
+       !p.sh_scales || !p.sh_bsplit || !p.sh_bimg || !p.ys || p.sh_scale_ld % 16 ||
+       p.sh_nck * 4 > p.sh_scale_ld))
+    return cudaErrorInvalidValue;
   if (gate_up)
     return launch_ex(L, dim3(grid), dim3(TC_THREADS), SMEM_BYTES, expert_tc_kernel<true>, wmap,
-                     smap, p);
+                     smap, shmap, p);
   return launch_ex(L, dim3(grid), dim3(TC_THREADS), SMEM_BYTES, expert_tc_kernel<false>, wmap,
-                   smap, p);
+                   smap, shmap, p);
 }
 
 }  // namespace mono

@@ -169,6 +169,16 @@ struct ExpertTcParams {
   uint8_t* tterms;         // gate_up: their term split, in down's layout
   uint8_t* tscales;
   float* y;                // down: outputs f32 [slots, rows_per_mat]
+  // down: the shared expert's down GEMM as extra items (sh_tiles = H / 128, 0: none): its
+  // weights by the launch's third map (e4m3 [H][Is], {128 B, 128 rows} boxes), E8M0 scales
+  // [H / 32][sh_scale_ld = Is / 32], t_s's split (common.cuh), rows sh_rows in sh_halves
+  // halves of at most 24, output y_s f32 [sh_rows, H]
+  int sh_tiles, sh_halves, sh_nck, sh_rows;
+  const uint8_t* sh_scales;
+  int sh_scale_ld;
+  const uint8_t* sh_bsplit;
+  const uint8_t* sh_bimg;
+  float* ys;
   float clamp;
   int* status;
 };
@@ -176,7 +186,8 @@ struct ExpertTcParams {
 // times the SM count)
 cudaError_t expert_tc_prepare(int* ctas_per_sm);
 cudaError_t launch_expert_tc(const Launch&, bool gate_up, const CUtensorMap& wmap,
-                             const CUtensorMap& smap, const ExpertTcParams& p, int grid);
+                             const CUtensorMap& smap, const CUtensorMap& shmap,
+                             const ExpertTcParams& p, int grid);
 
 // The dense MXFP8 GEMMs of many-row steps on the tensor cores (k_dense_tc.cu).  Weight map:
 // e4m3 [N rows][K bytes], 128-byte swizzle, {128 B, 128 rows} boxes; SwiGLU matrices (gate

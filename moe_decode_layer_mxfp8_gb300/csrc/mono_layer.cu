@@ -741,7 +741,14 @@ int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
                         h->buf<void>(MONO_BUF_TS), s.shared_inter, nullptr, Ls,
                         split_of(h, R, S_U), split_of(h, R, S_TS));
   }));
+  // Large steps with the shared expert on the tensor cores: its down GEMM runs inside the
+  // routed down launch (items ahead of the routed ones) instead of as its own launch -- on
+  // its own, its CTAs found no SM until the routed gate_up's persistent CTAs drained and then
+  // held up the routed down.  Its launch slot then stays empty (for the profiling events).
+  const bool sh_fused = tc && use_dense_tc(h, R, D_SHGU) && use_dense_tc(h, R, D_SHD) &&
+                        s.shared_inter % 512 == 0 && H % 128 == 0;
   TRY(run([&] {
+    if (sh_fused) return cudaSuccess;
     return dense_launch(h, D_SHD, R, h->buf<__half>(MONO_BUF_TS), s.shared_inter, EPI_F32,
                         h->buf<void>(MONO_BUF_YS), H, nullptr, Ls, split_of(h, R, S_TS));
   }));
@@ -770,7 +777,8 @@ int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
     p.tterms = h->t_terms;
     p.tscales = h->t_tscales;
     TRY(run([&] {
-      return launch_expert_tc(L, true, h->map_tc_gu, h->map_tc_gu_s, p, h->tc_ctas);
+      return launch_expert_tc(L, true, h->map_tc_gu, h->map_tc_gu_s, h->map_tc_gu, p,
+                              h->tc_ctas);
     }));
     p.K = s.moe_inter;
     p.rows_per_mat = H;
@@ -780,8 +788,22 @@ int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
     p.bterms = h->t_terms;
     p.bscales = h->t_tscales;
     p.y = h->buf<float>(MONO_BUF_YR);
+    if (sh_fused) {
+      p.sh_tiles = H / 128;
+      p.sh_rows = R;
+      p.sh_halves = (R + 23) / 24;
+      p.sh_nck = s.shared_inter / 128;
+      p.sh_scales = h->dense[D_SHD].scales;
+      p.sh_scale_ld = s.shared_inter / 32;
+      p.sh_bsplit = h->split[S_TS].data;
+      p.sh_bimg = h->split[S_TS].img;
+      p.ys = h->buf<float>(MONO_BUF_YS);
+      // its input, t_s's split, comes from the shared gate_up on the side stream
+      if (fork) TRY_CUDA(cudaStreamWaitEvent(stream, h->ev_join, 0));
+    }
     TRY(run([&] {
-      return launch_expert_tc(L, false, h->map_tc_d, h->map_tc_d_s, p, h->tc_ctas);
+      return launch_expert_tc(L, false, h->map_tc_d, h->map_tc_d_s, h->dense[D_SHD].tc_map, p,
+                              h->tc_ctas);
     }));
   } else {
     TRY(run([&] {
