@@ -57,6 +57,10 @@ struct NormArgs {
   // in common.cuh; rows <= 48)
   uint8_t* e4_data = nullptr;
   uint8_t* e4_img = nullptr;
+  // 1: the launch follows a kernel of the same step that is still running, so the kernel runs
+  // its output code once on no data (storing nothing) before griddepcontrol.wait, to have it
+  // in the instruction caches when the row arrives; 0 for a step's first launch
+  int warm = 0;
 };
 
 struct QkvNormInsertArgs {

@@ -953,6 +953,7 @@ int mono_layer_step(mono_layer_t* h, const mono_step_args* a, void* stream_ptr) 
   m.seam = {h->buf<__nv_bfloat16>(MONO_BUF_H), H, (const __nv_bfloat16*)h->w.ffn_norm, H, s.eps,
             h->buf<__half>(MONO_BUF_U), H};
   m.seam.status = h->status;
+  m.seam.warm = 1;  // wo_b is still running when its CTAs become resident
   m.x = x;
   m.positions = a->positions;
   m.R = R;
