@@ -221,52 +221,109 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  pdl_trigger();
   pdl_wait();
+  // Dependents are let in only now: everything the top-k wrote is complete, so the final
+  // combine may read the routing (and anything older) before its own wait.
+  pdl_trigger();
 
-  // routing metadata (written by the top-k kernel), checked, and the row groups
-  int n_hit = p.route->n_hit;
-  if (n_hit < 0 || n_hit > MAX_EXPERTS) {
-    if (tid == 0) atomicOr(p.status, ST_BAD_ROUTE);
-    n_hit = 0;
-  }
+  // Routing metadata (written by the top-k kernel), checked, and the row groups.  Every global
+  // read here is issued in one round -- the producer's first work item, the hit count, all
+  // MAX_EXPERTS entries of the hit arrays (those past the count are ignored) and the row map --
+  // so that the setup costs one memory latency, not a chain of them.
   // (staged in the ring's memory, which the pipeline does not use yet)
   int* ue = reinterpret_cast<int*>(smem);
   int* uoff = ue + MAX_EXPERTS;
   int* ucnt = uoff + MAX_EXPERTS;
-  for (int d = tid; d < n_hit; d += TC_THREADS) {
-    int e = p.route->hit_e[d], off = p.route->hit_off[d], cnt = p.route->hit_cnt[d];
-    if (e < 0 || e >= p.n_experts || cnt < 1 || off < 0 || off + cnt > p.n_slots) {
-      atomicOr(p.status, ST_BAD_ROUTE);
-      e = 0, off = 0, cnt = 1;
-    }
-    ue[d] = e, uoff[d] = off, ucnt[d] = cnt;
+  constexpr int HPT = (MAX_EXPERTS + TC_THREADS - 1) / TC_THREADS;  // hit entries per thread
+  constexpr int RPT = (MAX_SLOTS + TC_THREADS - 1) / TC_THREADS;    // row-map entries per thread
+  int q_first = 0;
+  if (tid == 0) q_first = atomicAdd(p.item_next, 1);
+  int n_hit = p.route->n_hit;
+  int he[HPT], ho[HPT], hc[HPT], rm[RPT];
+#pragma unroll
+  for (int k = 0; k < HPT; ++k) {
+    const int d = tid + k * TC_THREADS;
+    const bool in = d < MAX_EXPERTS;
+    he[k] = in ? p.route->hit_e[d] : 0;
+    ho[k] = in ? p.route->hit_off[d] : 0;
+    hc[k] = in ? p.route->hit_cnt[d] : 0;
   }
-  __syncthreads();
-  // the hit experts in decreasing row count (ties in expert order), so that the items of the
-  // largest groups, which stream slowest, are handed out first and the launch ends on short
-  // ones
-  for (int d = tid; d < n_hit; d += TC_THREADS) {
-    const int cd = ucnt[d];
-    int rank = 0;
-    for (int k = 0; k < n_hit; ++k) {
-      const int ck = ucnt[k];
-      rank += (ck > cd) | ((ck == cd) & (k < d));
+#pragma unroll
+  for (int k = 0; k < RPT; ++k) {
+    const int i = tid + k * TC_THREADS;
+    rm[k] = GU && i < p.n_slots ? p.rowmap[i] : 0;
+  }
+  if (n_hit < 0 || n_hit > MAX_EXPERTS) {
+    if (tid == 0) atomicOr(p.status, ST_BAD_ROUTE);
+    n_hit = 0;
+  }
+#pragma unroll
+  for (int k = 0; k < HPT; ++k) {
+    const int d = tid + k * TC_THREADS;
+    if (d < n_hit) {
+      int e = he[k], off = ho[k], cnt = hc[k];
+      if (e < 0 || e >= p.n_experts || cnt < 1 || off < 0 || off + cnt > p.n_slots) {
+        atomicOr(p.status, ST_BAD_ROUTE);
+        e = 0, off = 0, cnt = 1;
+      }
+      ue[d] = e, uoff[d] = off, ucnt[d] = cnt;
     }
-    rt.e[rank] = ue[d], rt.off[rank] = uoff[d], rt.cnt[rank] = cd;
   }
   if constexpr (GU) {
-    for (int i = tid; i < p.n_slots; i += TC_THREADS) {
-      int r = p.rowmap[i];
-      if (r < 0 || r >= p.act_rows) {
-        atomicOr(p.status, ST_BAD_ROUTE);
-        r = 0;
+#pragma unroll
+    for (int k = 0; k < RPT; ++k) {
+      const int i = tid + k * TC_THREADS;
+      if (i < p.n_slots) {
+        int r = rm[k];
+        if (r < 0 || r >= p.act_rows) {
+          atomicOr(p.status, ST_BAD_ROUTE);
+          r = 0;
+        }
+        rt.rowmap[i] = r;
       }
-      rt.rowmap[i] = r;
     }
   }
   __syncthreads();
-  if (warp == 0) {  // row-group prefix over the hit experts
+  if (warp == 0) {
+    // The hit experts in decreasing row count, so that the items of the largest groups, which
+    // stream slowest, are handed out first and the launch ends on short ones: a counting sort
+    // on min(count, 63), stable in expert order (every CTA must derive the same order, as the
+    // items are numbered across the launch), one warp over chunks of 32 experts.
+    int* pos0 = ucnt + MAX_EXPERTS;  // [64] bucket sizes, then each bucket's next position
+    pos0[lane] = 0;
+    pos0[lane + 32] = 0;
+    __syncwarp();
+    for (int d0 = 0; d0 < n_hit; d0 += 32) {
+      const int d = d0 + lane;
+      const int key = d < n_hit ? 63 - min(ucnt[d], 63) : 64;  // 64: no expert
+      const unsigned m = __match_any_sync(0xffffffffu, key);
+      if (key < 64 && lane == __ffs(m) - 1) pos0[key] += __popc(m);
+      __syncwarp();
+    }
+    {  // exclusive prefix over the 64 buckets, two a lane
+      const int h0 = pos0[2 * lane], h1 = pos0[2 * lane + 1];
+      int x = h0 + h1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      __syncwarp();
+      pos0[2 * lane] = x - h0 - h1;
+      pos0[2 * lane + 1] = x - h1;
+      __syncwarp();
+    }
+    for (int d0 = 0; d0 < n_hit; d0 += 32) {
+      const int d = d0 + lane;
+      const int key = d < n_hit ? 63 - min(ucnt[d], 63) : 64;
+      const unsigned m = __match_any_sync(0xffffffffu, key);
+      const int rank = key < 64 ? pos0[key] + __popc(m & ((1u << lane) - 1u)) : 0;
+      __syncwarp();
+      if (key < 64 && lane == __ffs(m) - 1) pos0[key] += __popc(m);
+      if (d < n_hit) rt.e[rank] = ue[d], rt.off[rank] = uoff[d], rt.cnt[rank] = ucnt[d];
+      __syncwarp();
+    }
+    // row-group prefix over the hit experts, in that order
     int carry = 0;
     for (int d0 = 0; d0 < n_hit; d0 += 32) {
       const int d = d0 + lane;
@@ -297,9 +354,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM)
   if (warp == 0) {
     // ---------------------------------------------------------------------------- producer
     int iter = 0;
-    int q = 0;
-    if (lane == 0) q = atomicAdd(p.item_next, 1);
-    q = __shfl_sync(0xffffffffu, q, 0);
+    int q = __shfl_sync(0xffffffffu, q_first, 0);  // (thread 0's, fetched with the routing)
     while (q < n_items) {
       int qn = 0;
       if (lane == 0) qn = atomicAdd(p.item_next, 1);

@@ -245,21 +245,25 @@ __global__ void __launch_bounds__(FINAL_THREADS) final_kernel(FinalArgs a) {
   const int r = blockIdx.x;
   const int c = blockIdx.y * FINAL_COLS + threadIdx.x * 8;
   const bool pad = a.positions[r] < 0;  // a step input: read before the wait
-  pdl_wait();
-  if (c >= a.H) return;
-  const size_t o = (size_t)r * a.H + c;
-  if (pad) {
-    *reinterpret_cast<uint4*>(a.out + o) = *reinterpret_cast<const uint4*>(a.x + o);
-    return;
-  }
+  const bool in = c < a.H;
+  const size_t o = (size_t)r * a.H + (in ? c : 0);
+  // Read before the wait as well: the routing and h.  The routed-expert kernels let their
+  // dependents in only after their own wait, when the top-k (and every earlier kernel, h's
+  // writer included) has completed; the expert outputs y_s and y_r are read after it.
   int pos[FINAL_MAX_K];
   float wj[FINAL_MAX_K];
 #pragma unroll
   for (int j = 0; j < FINAL_MAX_K; ++j) {
-    pos[j] = j < a.k ? a.slot_pos[r * a.k + j] : -1;
-    wj[j] = j < a.k ? a.topk_w[r * a.k + j] : 0.0f;
+    pos[j] = j < a.k && !pad ? a.slot_pos[r * a.k + j] : -1;
+    wj[j] = j < a.k && !pad ? a.topk_w[r * a.k + j] : 0.0f;
   }
-  const uint4 hv = *reinterpret_cast<const uint4*>(a.h + o);
+  const uint4 hv = in ? *reinterpret_cast<const uint4*>((pad ? a.x : a.h) + o) : uint4{};
+  pdl_wait();
+  if (!in) return;
+  if (pad) {
+    *reinterpret_cast<uint4*>(a.out + o) = hv;  // (x: the layer input)
+    return;
+  }
   const float4 s0 = *reinterpret_cast<const float4*>(a.ys + o);
   const float4 s1 = *reinterpret_cast<const float4*>(a.ys + o + 4);
   float4 y0[FINAL_MAX_K], y1[FINAL_MAX_K];

@@ -819,7 +819,9 @@ int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
                            h->buf<void>(MONO_BUF_YR), H, L);
     }));
   }
-  if (fork) TRY_CUDA(cudaStreamWaitEvent(stream, h->ev_join, 0));
+  // (with the shared down inside the routed down, that launch has already joined the side
+  // stream; a second join here would only keep the final combine from launching early)
+  if (fork && !sh_fused) TRY_CUDA(cudaStreamWaitEvent(stream, h->ev_join, 0));
   {
     FinalArgs f = {};
     f.x = m.x;

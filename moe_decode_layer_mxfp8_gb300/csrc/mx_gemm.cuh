@@ -945,29 +945,59 @@ __global__ void __launch_bounds__(gemm_threads(KS), FMT == 4 && KS == 1 ? 4 : 2)
     cluster_sync_all();
   else
     __syncthreads();
-  pdl_trigger();
+  // (the routed experts let their dependents in only after their own wait: the top-k is then
+  // complete, and the final combine reads the routing before its wait)
+  if (!L::EXPERT) pdl_trigger();
   // weights do not depend on the previous kernel: start streaming them before waiting on it
   int pre = 0;
   if (warp == CONSUMER_WARPS) pre = prefetch_weights<FMT, NT, NSTAGE, KS>(p, &map, smem, full);
   pdl_wait();
+  if (L::EXPERT) pdl_trigger();
   RouteSmem* rs = nullptr;
   if constexpr (L::EXPERT) {
     if (p.route) {
       rs = reinterpret_cast<RouteSmem*>(smem + L::ROUTE_OFF);
-      const int nh = min(p.route->n_hit, MAX_EXPERTS);
-      for (int i = threadIdx.x; i < nh; i += THREADS) {
-        rs->hit_e[i] = p.route->hit_e[i];
-        rs->hit_off[i] = p.route->hit_off[i];
-        rs->hit_cnt[i] = p.route->hit_cnt[i];
+      // every global read of the routing issued in one round (all MAX_EXPERTS entries, those
+      // past the hit count ignored), so that the copy costs one memory latency
+      constexpr int HPT = (MAX_EXPERTS + THREADS - 1) / THREADS;
+      constexpr int RPT = (MAX_SLOTS + THREADS - 1) / THREADS;
+      const int nh_raw = p.route->n_hit;
+      int he[HPT], ho[HPT], hc[HPT], g0[HPT], g1[HPT], rm[RPT];
+#pragma unroll
+      for (int k = 0; k < HPT; ++k) {
+        const int i = threadIdx.x + k * THREADS;
+        const bool in = i < MAX_EXPERTS;
+        he[k] = in ? p.route->hit_e[i] : 0;
+        ho[k] = in ? p.route->hit_off[i] : 0;
+        hc[k] = in ? p.route->hit_cnt[i] : 0;
+        g0[k] = in ? p.route->rg_prefix[i] : 0;
+        g1[k] = in ? p.route->rg_prefix[i + 1] : 0;
       }
-      for (int i = threadIdx.x; i <= nh; i += THREADS) rs->rg_prefix[i] = p.route->rg_prefix[i];
-      for (int i = threadIdx.x; i < nh; i += THREADS) {
-        const int g1 = min(p.route->rg_prefix[i + 1], MAX_SLOTS);
-        for (int g = p.route->rg_prefix[i]; g < g1; ++g) rs->rg_expert[g] = (uint8_t)i;
+#pragma unroll
+      for (int k = 0; k < RPT; ++k) {
+        const int i = threadIdx.x + k * THREADS;
+        rm[k] = p.act_rowmap && i < min(p.n_slots, MAX_SLOTS) ? p.act_rowmap[i] : 0;
       }
-      if (p.act_rowmap)
-        for (int i = threadIdx.x; i < min(p.n_slots, MAX_SLOTS); i += THREADS)
-          rs->rowmap[i] = p.act_rowmap[i];
+      const int nh = min(nh_raw, MAX_EXPERTS);
+#pragma unroll
+      for (int k = 0; k < HPT; ++k) {
+        const int i = threadIdx.x + k * THREADS;
+        if (i < nh) {
+          rs->hit_e[i] = he[k];
+          rs->hit_off[i] = ho[k];
+          rs->hit_cnt[i] = hc[k];
+          for (int g = g0[k]; g < min(g1[k], MAX_SLOTS); ++g) rs->rg_expert[g] = (uint8_t)i;
+        }
+        if (i <= nh && i < MAX_EXPERTS) rs->rg_prefix[i] = g0[k];
+        if (i == MAX_EXPERTS - 1 && nh == MAX_EXPERTS) rs->rg_prefix[MAX_EXPERTS] = g1[k];
+      }
+      if (p.act_rowmap) {
+#pragma unroll
+        for (int k = 0; k < RPT; ++k) {
+          const int i = threadIdx.x + k * THREADS;
+          if (i < min(p.n_slots, MAX_SLOTS)) rs->rowmap[i] = rm[k];
+        }
+      }
       if (threadIdx.x == 0) {
         rs->n_hit = nh;
         rs->tile_shift = (p.n_tiles & (p.n_tiles - 1)) == 0 ? __ffs(p.n_tiles) - 1 : -1;
