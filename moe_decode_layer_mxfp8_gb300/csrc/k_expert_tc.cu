@@ -175,17 +175,92 @@ __device__ __forceinline__ void sh_epilogue(const ExpertTcParams& p, const ShIte
   }
 }
 
+// The setup of every CTA: the step's routing (written by the top-k kernel) into rt -- the hit
+// experts in the order the items are handed out (decreasing row count) with the prefix of
+// their row groups, and gate_up's row map -- checked, and the producer's first work item
+// (thread 0's return value).  Every global read is issued in one round: the first work item,
+// the hit count, all MAX_EXPERTS entries of the ordered hit arrays (those past the count are
+// ignored) and the row map.  An entry that fails its check raises the status bit and leaves
+// this CTA without routed items.
+template <bool GU>
+__device__ __forceinline__ int tc_setup(const ExpertTcParams& p, TcRoute& rt, int* s_bad) {
+  const int tid = threadIdx.x;
+  constexpr int HPT = (MAX_EXPERTS + TC_THREADS - 1) / TC_THREADS;  // hit entries per thread
+  constexpr int RPT = (MAX_SLOTS + TC_THREADS - 1) / TC_THREADS;    // row-map entries per thread
+  static_assert(TC_ROWS == EXPERT_ROWS, "the top-k's row groups are the items' row groups");
+  if (tid == 0) *s_bad = 0;
+  int q_first = 0;
+  if (tid == 0) q_first = atomicAdd(p.item_next, 1);
+  int n_hit = p.route->n_hit;
+  int he[HPT], ho[HPT], hc[HPT], g0[HPT], g1[HPT], rm[RPT];
+#pragma unroll
+  for (int k = 0; k < HPT; ++k) {
+    const int d = tid + k * TC_THREADS;
+    const bool in = d < MAX_EXPERTS;
+    he[k] = in ? p.route->lpt_e[d] : 0;
+    ho[k] = in ? p.route->lpt_off[d] : 0;
+    hc[k] = in ? p.route->lpt_cnt[d] : 0;
+    g0[k] = in ? p.route->lpt_gpre[d] : 0;
+    g1[k] = in ? p.route->lpt_gpre[d + 1] : 0;
+  }
+#pragma unroll
+  for (int k = 0; k < RPT; ++k) {
+    const int i = tid + k * TC_THREADS;
+    rm[k] = GU && i < p.n_slots ? p.rowmap[i] : 0;
+  }
+  bool bad = n_hit < 0 || n_hit > MAX_EXPERTS;
+  if (bad) n_hit = 0;
+  __syncthreads();  // (s_bad cleared)
+#pragma unroll
+  for (int k = 0; k < HPT; ++k) {
+    const int d = tid + k * TC_THREADS;
+    if (d < n_hit) {
+      const int e = he[k], off = ho[k], cnt = hc[k];
+      bad |= e < 0 || e >= p.n_experts || cnt < 1 || off < 0 || off + cnt > p.n_slots ||
+             g0[k] < 0 || g1[k] - g0[k] != (cnt + TC_ROWS - 1) / TC_ROWS || g1[k] > MAX_GROUPS;
+      rt.e[d] = e, rt.off[d] = off, rt.cnt[d] = cnt, rt.gpre[d] = g0[k];
+      if (d == n_hit - 1) rt.gpre[n_hit] = g1[k];
+    }
+  }
+  if (GU) {
+#pragma unroll
+    for (int k = 0; k < RPT; ++k) {
+      const int i = tid + k * TC_THREADS;
+      if (i < p.n_slots) {
+        bad |= rm[k] < 0 || rm[k] >= p.act_rows;
+        rt.rowmap[i] = rm[k];
+      }
+    }
+  }
+  if (bad) *s_bad = 1;
+  __syncthreads();
+  if (*s_bad) {
+    if (tid == 0) atomicOr(p.status, ST_BAD_ROUTE);
+    n_hit = 0;
+  }
+  if (tid == 0) {
+    rt.n_hit = n_hit;
+    if (n_hit == 0) rt.gpre[0] = 0;
+  }
+  for (int d = tid; d < n_hit; d += TC_THREADS)
+    for (int g = rt.gpre[d]; g < rt.gpre[d + 1]; ++g) rt.gexp[g] = (uint8_t)d;
+  __syncthreads();
+  return q_first;
+}
+
 template <bool GU>
 __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM)
     expert_tc_kernel(const __grid_constant__ CUtensorMap wmap,
                      const __grid_constant__ CUtensorMap smap,
-                     const __grid_constant__ CUtensorMap shmap, const ExpertTcParams p) {
+                     const __grid_constant__ CUtensorMap shmap,
+                     const __grid_constant__ ExpertTcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[NSTAGE], empty[NSTAGE], tfull[2], tempty[2], drain;
   __shared__ __align__(8) uint64_t xfull[2], xempty[2];  // gate_up: the up-value exchange
   __shared__ TcRoute rt;
+  __shared__ int s_bad;
   __shared__ int slot_q[NSTAGE], acc_q[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -225,127 +300,8 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM)
   // Dependents are let in only now: everything the top-k wrote is complete, so the final
   // combine may read the routing (and anything older) before its own wait.
   pdl_trigger();
-
-  // Routing metadata (written by the top-k kernel), checked, and the row groups.  Every global
-  // read here is issued in one round -- the producer's first work item, the hit count, all
-  // MAX_EXPERTS entries of the hit arrays (those past the count are ignored) and the row map --
-  // so that the setup costs one memory latency, not a chain of them.
-  // (staged in the ring's memory, which the pipeline does not use yet)
-  int* ue = reinterpret_cast<int*>(smem);
-  int* uoff = ue + MAX_EXPERTS;
-  int* ucnt = uoff + MAX_EXPERTS;
-  constexpr int HPT = (MAX_EXPERTS + TC_THREADS - 1) / TC_THREADS;  // hit entries per thread
-  constexpr int RPT = (MAX_SLOTS + TC_THREADS - 1) / TC_THREADS;    // row-map entries per thread
-  int q_first = 0;
-  if (tid == 0) q_first = atomicAdd(p.item_next, 1);
-  int n_hit = p.route->n_hit;
-  int he[HPT], ho[HPT], hc[HPT], rm[RPT];
-#pragma unroll
-  for (int k = 0; k < HPT; ++k) {
-    const int d = tid + k * TC_THREADS;
-    const bool in = d < MAX_EXPERTS;
-    he[k] = in ? p.route->hit_e[d] : 0;
-    ho[k] = in ? p.route->hit_off[d] : 0;
-    hc[k] = in ? p.route->hit_cnt[d] : 0;
-  }
-#pragma unroll
-  for (int k = 0; k < RPT; ++k) {
-    const int i = tid + k * TC_THREADS;
-    rm[k] = GU && i < p.n_slots ? p.rowmap[i] : 0;
-  }
-  if (n_hit < 0 || n_hit > MAX_EXPERTS) {
-    if (tid == 0) atomicOr(p.status, ST_BAD_ROUTE);
-    n_hit = 0;
-  }
-#pragma unroll
-  for (int k = 0; k < HPT; ++k) {
-    const int d = tid + k * TC_THREADS;
-    if (d < n_hit) {
-      int e = he[k], off = ho[k], cnt = hc[k];
-      if (e < 0 || e >= p.n_experts || cnt < 1 || off < 0 || off + cnt > p.n_slots) {
-        atomicOr(p.status, ST_BAD_ROUTE);
-        e = 0, off = 0, cnt = 1;
-      }
-      ue[d] = e, uoff[d] = off, ucnt[d] = cnt;
-    }
-  }
-  if constexpr (GU) {
-#pragma unroll
-    for (int k = 0; k < RPT; ++k) {
-      const int i = tid + k * TC_THREADS;
-      if (i < p.n_slots) {
-        int r = rm[k];
-        if (r < 0 || r >= p.act_rows) {
-          atomicOr(p.status, ST_BAD_ROUTE);
-          r = 0;
-        }
-        rt.rowmap[i] = r;
-      }
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // The hit experts in decreasing row count, so that the items of the largest groups, which
-    // stream slowest, are handed out first and the launch ends on short ones: a counting sort
-    // on min(count, 63), stable in expert order (every CTA must derive the same order, as the
-    // items are numbered across the launch), one warp over chunks of 32 experts.
-    int* pos0 = ucnt + MAX_EXPERTS;  // [64] bucket sizes, then each bucket's next position
-    pos0[lane] = 0;
-    pos0[lane + 32] = 0;
-    __syncwarp();
-    for (int d0 = 0; d0 < n_hit; d0 += 32) {
-      const int d = d0 + lane;
-      const int key = d < n_hit ? 63 - min(ucnt[d], 63) : 64;  // 64: no expert
-      const unsigned m = __match_any_sync(0xffffffffu, key);
-      if (key < 64 && lane == __ffs(m) - 1) pos0[key] += __popc(m);
-      __syncwarp();
-    }
-    {  // exclusive prefix over the 64 buckets, two a lane
-      const int h0 = pos0[2 * lane], h1 = pos0[2 * lane + 1];
-      int x = h0 + h1;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      __syncwarp();
-      pos0[2 * lane] = x - h0 - h1;
-      pos0[2 * lane + 1] = x - h1;
-      __syncwarp();
-    }
-    for (int d0 = 0; d0 < n_hit; d0 += 32) {
-      const int d = d0 + lane;
-      const int key = d < n_hit ? 63 - min(ucnt[d], 63) : 64;
-      const unsigned m = __match_any_sync(0xffffffffu, key);
-      const int rank = key < 64 ? pos0[key] + __popc(m & ((1u << lane) - 1u)) : 0;
-      __syncwarp();
-      if (key < 64 && lane == __ffs(m) - 1) pos0[key] += __popc(m);
-      if (d < n_hit) rt.e[rank] = ue[d], rt.off[rank] = uoff[d], rt.cnt[rank] = ucnt[d];
-      __syncwarp();
-    }
-    // row-group prefix over the hit experts, in that order
-    int carry = 0;
-    for (int d0 = 0; d0 < n_hit; d0 += 32) {
-      const int d = d0 + lane;
-      const int v = d < n_hit ? (rt.cnt[d] + TC_ROWS - 1) / TC_ROWS : 0;
-      int x = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      if (d < n_hit) rt.gpre[d] = carry + x - v;
-      carry += __shfl_sync(0xffffffffu, x, 31);
-    }
-    if (lane == 0) {
-      rt.gpre[n_hit] = carry;
-      rt.n_hit = n_hit;
-    }
-  }
-  __syncthreads();
-  for (int d = tid; d < n_hit; d += TC_THREADS)
-    for (int g = rt.gpre[d]; g < rt.gpre[d + 1] && g < MAX_GROUPS; ++g) rt.gexp[g] = (uint8_t)d;
-  __syncthreads();
+  const int q_first = tc_setup<GU>(p, rt, &s_bad);
+  const int n_hit = rt.n_hit;
   // the shared expert's down items come first (each streams p.sh_nck stages, more than a
   // routed item's), then the routed items
   const int n_sh = GU ? 0 : p.sh_tiles * p.sh_halves;
@@ -356,8 +312,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM)
     int iter = 0;
     int q = __shfl_sync(0xffffffffu, q_first, 0);  // (thread 0's, fetched with the routing)
     while (q < n_items) {
-      int qn = 0;
-      if (lane == 0) qn = atomicAdd(p.item_next, 1);
+      int qn = 0;  // the next item, fetched once this one's first stage is on its way
       if (!GU && q < n_sh) {
         const ShItem si = sh_item(p, q);
         for (int c = 0; c < p.sh_nck; ++c, ++iter) {
@@ -368,6 +323,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM)
             if (c == 0) slot_q[s] = q;  // published by the arrival in sh_issue
             sh_issue(p, &shmap, si, c, smem + s * STAGE, &full[s]);
           }
+          if (c == 0 && lane == 0) qn = atomicAdd(p.item_next, 1);
           __syncwarp();
         }
         q = __shfl_sync(0xffffffffu, qn, 0);
@@ -405,6 +361,7 @@ __global__ void __launch_bounds__(TC_THREADS, TC_CTAS_PER_SM)
                         p.bterms + rc * (ACT_TERMS * TERM_ROW), ACT_TERMS * TERM_ROW, &full[s]);
           bulk_load_g2s(st + SB_OFF + lane * TERM_SC, p.bscales + rc * TERM_SC, TERM_SC, &full[s]);
         }
+        if (c == 0 && lane == 0) qn = atomicAdd(p.item_next, 1);
       }
       q = __shfl_sync(0xffffffffu, qn, 0);
     }

@@ -165,10 +165,16 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
   __shared__ int s_pos[MAX_ROWS];
   __shared__ unsigned long long s_mask[MAX_EXPERTS];  // rows routed to each expert
   __shared__ int s_tot[3][MAX_EXPERTS / 32];          // per-warp totals of the expert scans
+  // the hit experts by key = 63 - row count (a bit per expert), and per key the experts and the
+  // row groups of all smaller keys
+  __shared__ unsigned s_kmask[64][MAX_EXPERTS / 32];
+  __shared__ int s_kstart[64], s_kgrp[64];
+  static_assert(MAX_ROWS < 63, "a row count fits a key");
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int NW = TOPK_THREADS / 32;
   for (int e = tid; e < MAX_EXPERTS; e += TOPK_THREADS) s_mask[e] = 0ull;
+  for (int i = tid; i < 64 * (MAX_EXPERTS / 32); i += TOPK_THREADS) (&s_kmask[0][0])[i] = 0u;
   if (tid < a.rows) s_pos[tid] = a.positions[tid];  // a step input: read before the wait
   if (warp == 0) {  // warm the selection code while the previous kernel finishes
     const Pick dry = select_topk(s_z, a.E, a.k, a.E <= 128 ? 8 : 16, lane & 7, false);
@@ -246,8 +252,29 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
       if (lane >= o) ic += tc, ih += th, ir += tr;
     }
     if (lane == 31) s_tot[0][warp] = ic, s_tot[1][warp] = ih, s_tot[2][warp] = ir;
+    if (a.lpt && c > 0) atomicOr(&s_kmask[63 - c][e >> 5], 1u << (e & 31));
   }
   __syncthreads();
+  static_assert(SW < NW, "a spare warp for the key prefix");
+  if (a.lpt && warp == SW) {  // per key: the experts and the row groups of all smaller keys
+    int n[2], g[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int key = 2 * lane + i;
+      n[i] = 0;
+#pragma unroll
+      for (int w = 0; w < MAX_EXPERTS / 32; ++w) n[i] += __popc(s_kmask[key][w]);
+      g[i] = n[i] * ((63 - key + EXPERT_ROWS - 1) / EXPERT_ROWS);
+    }
+    int xn = n[0] + n[1], xg = g[0] + g[1];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int yn = __shfl_up_sync(0xffffffffu, xn, o), yg = __shfl_up_sync(0xffffffffu, xg, o);
+      if (lane >= o) xn += yn, xg += yg;
+    }
+    s_kstart[2 * lane] = xn - n[0] - n[1], s_kstart[2 * lane + 1] = xn - n[1];
+    s_kgrp[2 * lane] = xg - g[0] - g[1], s_kgrp[2 * lane + 1] = xg - g[1];
+  }
   __shared__ int s_off[MAX_EXPERTS];
   if (warp < SW) {
     int bo = 0, bh = 0, br = 0;
@@ -263,9 +290,21 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
     if (warp == SW - 1 && lane == 31) {
       a.route->n_hit = bh + ih;
       a.route->rg_prefix[bh + ih] = br + ir;
+      if (a.lpt) a.route->lpt_gpre[bh + ih] = br + ir;
     }
   }
   __syncthreads();
+  // phase 2b: the hit experts in decreasing row count, ties in expert order: an expert's
+  // place is its key's start plus the experts of its key below it
+  if (a.lpt && warp < SW && c > 0) {
+    const int key = 63 - c, w0 = e >> 5;
+    int rank = s_kstart[key] + __popc(s_kmask[key][w0] & ((1u << (e & 31)) - 1u));
+    for (int w = 0; w < w0; ++w) rank += __popc(s_kmask[key][w]);
+    a.route->lpt_e[rank] = e;
+    a.route->lpt_off[rank] = s_off[e];
+    a.route->lpt_cnt[rank] = c;
+    a.route->lpt_gpre[rank] = s_kgrp[key] + (rank - s_kstart[key]) * rg;
+  }
   // phase 3: stable placement -- an expert's entries in row order (a row picks an expert once)
   const int n = a.rows * a.k;
   for (int q = tid; q < n; q += TOPK_THREADS) {

@@ -122,6 +122,7 @@ struct TopkArgs {
   int* user_idx;
   float* user_w;
   int* status;
+  int lpt;  // 1: also write the hit experts in decreasing row count (RouteInfo::lpt_*)
 };
 
 struct FinalArgs {

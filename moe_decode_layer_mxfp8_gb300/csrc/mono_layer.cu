@@ -733,6 +733,7 @@ int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
     t.user_idx = m.topk_idx_out;
     t.user_w = m.topk_w_out;
     t.status = h->status;
+    t.lpt = tc ? 1 : 0;  // the tensor-core expert launches hand out items in that order
     TRY(run([&] { return launch_topk(L, t); }));
   }
   if (fork) TRY_CUDA(cudaStreamWaitEvent(h->side, h->ev_fork, 0));

@@ -56,6 +56,10 @@ struct RouteInfo {
   int hit_cnt[MAX_EXPERTS];        // number of rows routed to it
   int rg_prefix[MAX_EXPERTS + 1];  // prefix sum of ceil(hit_cnt / EXPERT_ROWS)
   int item_next[2];                // work counters of the large-step gate_up / down launches
+  // The same hit experts in decreasing row count (ties in expert order): the order in which
+  // the large-step launches hand out their items, largest groups first.
+  int lpt_e[MAX_EXPERTS], lpt_off[MAX_EXPERTS], lpt_cnt[MAX_EXPERTS];
+  int lpt_gpre[MAX_EXPERTS + 1];   // prefix sum of ceil(lpt_cnt / EXPERT_ROWS)
 };
 
 // Shared-memory copy of the routing metadata plus the activation row map, and the hit
