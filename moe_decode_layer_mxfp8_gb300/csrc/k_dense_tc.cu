@@ -82,6 +82,12 @@ __device__ __forceinline__ void owner_epilogue(const DenseTcParams& p, const flo
     const bool ok = !dry && col < ncols;
     const float* q0 =
         KS > 1 ? recv + (lb * KS * brows + lane) * EP_LD : recv + (32 * b + lane) * EP_LD;
+    float rv[U];  // the residual first: its loads are in flight while the slots are added
+    if (EPI == EPI_RESID_BF16)
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        rv[u] = ok ? __bfloat162float(p.resid[(size_t)min(i0 + u, R - 1) * p.resid_ld + col])
+                   : 0.0f;
     float s[U], su[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) s[u] = su[u] = 0.0f;
@@ -93,12 +99,6 @@ __device__ __forceinline__ void owner_epilogue(const DenseTcParams& p, const flo
         s[u] += q[0];
         if (SW) su[u] += q[up];
       }
-    float rv[U];
-    if (EPI == EPI_RESID_BF16)
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        rv[u] = ok ? __bfloat162float(p.resid[(size_t)min(i0 + u, R - 1) * p.resid_ld + col])
-                   : 0.0f;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int i = i0 + u;
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(DT_THREADS, 1)
                                              ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t afull[DT_NST], bfull[DT_NST], empty[DT_NST], done, drain;
   __shared__ __align__(8) uint64_t aimg_ready;  // the weight-scale images are written
-  __shared__ __align__(8) uint64_t red_ready, red_full, red_done;
+  __shared__ __align__(8) uint64_t red_ready, red_full;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   volatile int* abort = &s_abort;
@@ -184,7 +184,6 @@ __global__ void __launch_bounds__(DT_THREADS, 1)
     mbar_init(&aimg_ready, 4);  // one arrival per image-writing warp
     mbar_init(&red_ready, min(sw ? 2 : 4, ks));  // each owner's rings are free to receive
     mbar_init(&red_full, 1);  // the owner's expect_tx arrival; the pushed blocks complete_tx
-    mbar_init(&red_done, ks);
     *abort = 0;
     fence_mbar_init();
     prefetch_tmap(&wmap);
@@ -354,14 +353,10 @@ __global__ void __launch_bounds__(DT_THREADS, 1)
   }
   owner_epilogue_ks(p, recv, tile, (int)rank, nown, warp, lane, false);
 finish:
-  if (ks > 1) {
-    // this CTA's pushes have read its partial tile, and no CTA of the cluster leaves while
-    // another may still push into it
-    if (tid == 0) bulk_wait_read();
-    __syncthreads();
-    if (tid < ks) mbar_arrive_remote(mapa_shared(smem_u32(&red_done), (uint32_t)tid));
-    warp_wait(&red_done, 0, p.status, abort);
-  }
+  // A CTA leaves once its pushes have read its partial tile: every push into an owner has
+  // landed when its receive barrier completes, before its epilogue, and a CTA that owns no
+  // block receives none (so no cluster-wide handshake at the end).
+  if (ks > 1 && tid == 0) bulk_wait_read();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
