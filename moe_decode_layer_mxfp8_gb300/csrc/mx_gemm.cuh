@@ -876,7 +876,11 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
       owner_epilogue_any<L::EP_LD, NTHR>(p, it, recv, tid, rank);
       if (tid == 0) bulk_wait_read();  // this CTA's pushes have read its partial tile
       consumer_bar<NTHR>();
-      if (tid < p.ksplit) mbar_arrive_remote(mapa_shared(smem_u32(red_done), tid));  // tile free
+      // tile free -- announced only when another tile follows: the CTAs of a cluster take the
+      // same tiles, so after the last one nobody pushes again, and no CTA then touches a peer's
+      // shared memory (each has received all of its slots before its epilogue)
+      if (q + (int)gridDim.x < n_items && tid < p.ksplit)
+        mbar_arrive_remote(mapa_shared(smem_u32(red_done), tid));
     } else if constexpr (KS == 1 && FMT == 4) {
       if (*abort) return;
       epilogue_regs<NT>(p, it, acc, rowA, rowB, c, pair_gu);
@@ -910,8 +914,6 @@ __device__ void gemm_consumer(const GemmParams& p, const RouteSmem* rs, uint8_t*
     }
     ++tiles_done;
   }
-  // no peer may still be reading this CTA's shared memory when it exits
-  if (clustered && tiles_done > 0) pipe_wait<true>(red_done, (tiles_done - 1) & 1, p.status, abort);
 }
 
 template <int FMT, int NT, int NSTAGE, int KS>
