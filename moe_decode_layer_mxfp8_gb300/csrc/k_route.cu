@@ -1,7 +1,7 @@
 // Router and expert grouping ("Mono decode layer for DeepSeek-V4.1-Flash on MI355X", launch
 // table K2: "router, top-6"; ATOM changes: "f32 router logits").
 //
-// router_kernel: z[r, e] = u[r] . W_r[e] in f32, split over K: CTA (4 experts x 2 warps,
+// router_kernel: z[r, e] = u[r] . W_r[e] in f32, split over K: CTA (8 experts x 2 warps,
 // 1024-wide K slice, 16 rows) holds its experts' weight slices in registers (fetched before
 // waiting on the previous kernel), stages the slice of its rows of u in shared memory and
 // writes one partial per (slice, row, expert).  Rows go eight at a time: eight independent FMA chains
@@ -20,7 +20,7 @@ namespace mono {
 
 namespace {
 
-constexpr int RT_EXPERTS = 4;    // experts per CTA
+constexpr int RT_EXPERTS = 8;    // experts per CTA
 constexpr int RT_HALVES = 2;     // warps per expert, taking alternate groups of 8 rows
 constexpr int RT_THREADS = RT_EXPERTS * RT_HALVES * 32;
 constexpr int RT_J = ROUTER_KSLICE / 128;  // float4 weight chunks per lane
