@@ -257,7 +257,7 @@ def measure_device(name, steps, warmup, dev, n_copies, sampler=None):
     res = dict(spec=spec, step=step, layers=layers, outs=outs, stream=stream, us=us, ms=ms,
                dist=dist,
                bytes=avg_bytes, bytes_detail=byte_list[0], d_hit=[b["d_hit"] for b in byte_list],
-               launches=steps * layers[0][0].launches_per_step(), copies=C)
+               launches=steps * layers[0][0].kernels_last_step(), copies=C)
     return res
 
 
@@ -671,7 +671,7 @@ def schedule_probe():
 
 
 def run_eager(name, n):
-    """N eager layer steps (launch order: per step 15 launches, see mono_layer_launch_name)."""
+    """N eager layer steps (launch order: per step the slots of mono_layer_launch_name)."""
     from moe_decode_layer_mxfp8_gb300 import build
     build.build()
     dev = torch.device("cuda", 0)

@@ -231,8 +231,14 @@ int mono_layer_buffer(mono_layer_t *h, int which, void **dev_ptr, size_t *bytes)
  * device has finished).  `bytes` may be smaller than the buffer. */
 int mono_layer_read_buffer(mono_layer_t *h, int which, void *host_dst, size_t bytes);
 
-/* Number of kernel launches one mono_layer_step enqueues. */
+/* Number of launch slots of a step: the profiling events below bracket each slot.  A slot
+ * that the step's size does not use launches nothing (mono_layer_kernels_last_step counts the
+ * kernels actually enqueued). */
 int mono_layer_launches_per_step(mono_layer_t *h);
+
+/* Number of kernels the last mono_layer_step or mono_ffn_step call on this handle enqueued
+ * (0 before the first call). */
+int mono_layer_kernels_last_step(mono_layer_t *h);
 
 /* Short name of the i-th launch of a step ("attn_norm", "wqkv", ...), or NULL. */
 const char *mono_layer_launch_name(int i);

@@ -61,7 +61,8 @@ class FfnArgs(C.Structure):
 EXPORTS = ["mono_layer_build", "mono_layer_step", "mono_ffn_step", "mono_layer_status",
            "mono_layer_free",
            "mono_layer_strerror", "mono_layer_buffer", "mono_layer_read_buffer",
-           "mono_layer_launches_per_step", "mono_layer_launch_name",
+           "mono_layer_launches_per_step", "mono_layer_kernels_last_step",
+           "mono_layer_launch_name",
            "mono_layer_set_profile_events", "mono_attention_noalloc",
            "mono_layer_selftest_wait_timeout"]
 
@@ -94,6 +95,7 @@ def lib() -> C.CDLL:
                                         C.POINTER(C.c_size_t)]
         L.mono_layer_read_buffer.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_size_t]
         L.mono_layer_launches_per_step.argtypes = [C.c_void_p]
+        L.mono_layer_kernels_last_step.argtypes = [C.c_void_p]
         L.mono_layer_launch_name.argtypes = [C.c_int]
         L.mono_layer_launch_name.restype = C.c_char_p
         L.mono_layer_set_profile_events.argtypes = [C.c_void_p, C.c_void_p, C.c_int]
@@ -214,6 +216,10 @@ class Layer:
 
     def launches_per_step(self) -> int:
         return lib().mono_layer_launches_per_step(self._h)
+
+    def kernels_last_step(self) -> int:
+        """Kernels the last step call on this layer enqueued (empty launch slots excluded)."""
+        return lib().mono_layer_kernels_last_step(self._h)
 
     def launch_names(self) -> list[str]:
         return [lib().mono_layer_launch_name(i).decode() for i in range(self.launches_per_step())]

@@ -73,6 +73,7 @@ struct mono_layer {
   // the shared expert runs on a second stream, concurrently with the router and top-k
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  int kernels_last = 0;  // kernels the last step call enqueued
   int* status = nullptr;
   RouteInfo* route = nullptr;
   int* perm = nullptr;
@@ -526,6 +527,8 @@ int mono_layer_read_buffer(mono_layer_t* h, int which, void* host_dst, size_t by
 
 int mono_layer_launches_per_step(mono_layer_t* h) { return h ? kLaunchesPerStep : MONO_ERR_INVALID_ARG; }
 
+int mono_layer_kernels_last_step(mono_layer_t* h) { return h ? h->kernels_last : MONO_ERR_INVALID_ARG; }
+
 const char* mono_layer_launch_name(int i) {
   return (i >= 0 && i < kLaunchesPerStep) ? kLaunchNames[i] : nullptr;
 }
@@ -554,16 +557,24 @@ namespace {
 struct Enqueue {
   mono_layer* h;
   cudaStream_t stream;
-  int next;  // launch index (into the layer's launch-name list) of the next launch
+  int next;      // launch index (into the layer's launch-name list) of the next launch
+  int kernels = 0;  // kernels enqueued so far
   template <class F>
   int operator()(F&& launch) {
+    const int rc = skip();
+    if (rc != MONO_OK) return rc;
+    ++kernels;
+    const cudaError_t e = launch();
+    return e == cudaSuccess ? MONO_OK : cuda_fail(e);
+  }
+  // a slot this step leaves empty (its profiling event is still recorded)
+  int skip() {
     if (h->profiling) {
       const cudaError_t e = cudaEventRecord(h->prof[next], stream);
       if (e != cudaSuccess) return cuda_fail(e);
     }
     ++next;
-    const cudaError_t e = launch();
-    return e == cudaSuccess ? MONO_OK : cuda_fail(e);
+    return MONO_OK;
   }
 };
 
@@ -748,11 +759,14 @@ int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
   // held up the routed down.  Its launch slot then stays empty (for the profiling events).
   const bool sh_fused = tc && use_dense_tc(h, R, D_SHGU) && use_dense_tc(h, R, D_SHD) &&
                         s.shared_inter % 512 == 0 && H % 128 == 0;
-  TRY(run([&] {
-    if (sh_fused) return cudaSuccess;
-    return dense_launch(h, D_SHD, R, h->buf<__half>(MONO_BUF_TS), s.shared_inter, EPI_F32,
-                        h->buf<void>(MONO_BUF_YS), H, nullptr, Ls, split_of(h, R, S_TS));
-  }));
+  if (sh_fused) {
+    TRY(run.skip());
+  } else {
+    TRY(run([&] {
+      return dense_launch(h, D_SHD, R, h->buf<__half>(MONO_BUF_TS), s.shared_inter, EPI_F32,
+                          h->buf<void>(MONO_BUF_YS), H, nullptr, Ls, split_of(h, R, S_TS));
+    }));
+  }
   if (fork) TRY_CUDA(cudaEventRecord(h->ev_join, h->side));
   // The routed experts start right after the top-k and the shared expert joins before the
   // final combine.  (Small steps' routed clusters take their items statically; those placed
@@ -839,6 +853,7 @@ int enqueue_moe(mono_layer* h, const MoeIn& m, Enqueue& run) {
     TRY(run([&] { return launch_final(L, f); }));
   }
   if (h->profiling) TRY_CUDA(cudaEventRecord(h->prof[kLaunchesPerStep], stream));
+  h->kernels_last = run.kernels;
   return MONO_OK;
 }
 

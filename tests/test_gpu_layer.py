@@ -231,6 +231,16 @@ def test_empty_step_is_refused_and_the_next_step_runs():
     assert np.array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), g["out"])
 
 
+@pytest.mark.parametrize("name,kernels", [("small_r11", 15), ("full_r48", 14)])
+def test_kernels_last_step_counts_the_launched_kernels(name, kernels):
+    """Every launch slot runs a kernel at small steps; at large steps the shared expert's
+    down GEMM runs inside the routed down launch, so its slot launches nothing."""
+    spec, wn, sn, g, layer, wd, sd = _case(name)
+    assert layer.launches_per_step() == 15
+    run_step(layer, spec, sd, sd["x"].shape[0])
+    assert layer.kernels_last_step() == kernels
+
+
 @pytest.mark.parametrize("name", ["small_r11", "full_r48"])
 def test_all_pad_rows_pass_x_through(name):
     """The degenerate step: every row a pad row.  Pad rows leave the layer unchanged
