@@ -429,6 +429,34 @@ __device__ __forceinline__ void split_terms_x8(const float (&v)[8], uint32_t (&w
   }
 }
 
+// The same split for a block held four consecutive values per lane by an aligned group of 8
+// lanes: words[t] = this lane's 4 codes of term t in the low 16 bits (element 2i in the low
+// nibble of byte i).
+__device__ __forceinline__ void split_terms_x4(const float (&v)[4], uint32_t (&words)[ACT_TERMS],
+                                               uint32_t (&codes)[ACT_TERMS]) {
+  float r[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+  for (int t = 0; t < ACT_TERMS; ++t) {
+    float a = fmaxf(fmaxf(fabsf(r[0]), fabsf(r[1])), fmaxf(fabsf(r[2]), fabsf(r[3])));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+    const uint32_t code = e2m1_term_code(a);
+    const float inv = e8m0_inv_pow2(code), sc = e8m0_pow2(code);
+    const uint32_t w = e2m1x2_of(r[0] * inv, r[1] * inv) | (e2m1x2_of(r[2] * inv, r[3] * inv) << 8);
+    uint32_t h0, h1;
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %2;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n}"
+        : "=r"(h0), "=r"(h1)
+        : "r"(w));
+    const float2 q0 = __half22float2(*reinterpret_cast<const __half2*>(&h0));
+    const float2 q1 = __half22float2(*reinterpret_cast<const __half2*>(&h1));
+    r[0] -= q0.x * sc, r[1] -= q0.y * sc, r[2] -= q1.x * sc, r[3] -= q1.y * sc;
+    words[t] = w;
+    codes[t] = code;
+  }
+}
+
 // The same split for a 32-element block held one value per lane by a whole warp: words[t]
 // = the codes of the 8-lane group this lane belongs to (lanes 8k .. 8k + 7 give bytes 0 .. 3
 // of word k), codes[t] = the term's scale code.
@@ -546,6 +574,36 @@ __device__ __forceinline__ void split_store8(const float (&v)[8], bool in, int r
     if ((k8 & 31) == 0) {
       img[split_img_off(row, k8)] = (uint8_t)code;
       img[split_img_off(SPLIT_LO + row, k8)] = (uint8_t)code;
+    }
+  }
+}
+
+// The e4m3 split of a block held four consecutive elements per lane by an aligned group of 8
+// lanes (k4 = the first element, a multiple of 4): every lane of the warp calls it.
+__device__ __forceinline__ void split_store4(const float (&v)[4], bool in, int row, int k4,
+                                             uint8_t* data, uint8_t* img) {
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) a = fmaxf(a, in ? fabsf(v[i]) : 0.0f);
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+  a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
+  const uint32_t code = e4m3_block_code(a);
+  const float inv = e8m0_inverse(code);
+  uint32_t h = 0, l = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t hb, lb;
+    e4m3_hilo(in ? v[i] * inv : 0.0f, hb, lb);
+    h |= hb << (8 * i);
+    l |= lb << (8 * i);
+  }
+  if (in) {
+    *reinterpret_cast<uint32_t*>(data + split_off(row, k4)) = h;
+    *reinterpret_cast<uint32_t*>(data + split_off(SPLIT_LO + row, k4)) = l;
+    if ((k4 & 31) == 0) {
+      img[split_img_off(row, k4)] = (uint8_t)code;
+      img[split_img_off(SPLIT_LO + row, k4)] = (uint8_t)code;
     }
   }
 }

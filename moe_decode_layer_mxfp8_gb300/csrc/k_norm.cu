@@ -14,72 +14,77 @@ namespace {
 constexpr int NORM_THREADS = 256;
 constexpr int NORM_CHUNKS = 4;  // 8-element chunks per thread: rows up to 8192 wide
 
-// RMSNorm: CTA (row r, column slice y) writes output chunk q = RMS_THREADS y + t from thread
-// t, after computing the whole row's sum of squares itself (each of the row's CTAs reads the
-// whole row; the row is in L2).  Spreading a row over several CTAs spreads the output work,
-// the splits' serial per-block steps above all, over more SMs.
-constexpr int RMS_THREADS = 128;
-constexpr int RMS_CHUNKS = 8;  // 8-element chunks per thread of the sum: rows up to 8192 wide
+// RMSNorm: CTA (row r, 1024-column slice y) writes output elements 4q .. 4q + 3, q =
+// RMS_THREADS y + t, from thread t, after computing the whole row's sum of squares itself (each
+// of the row's CTAs reads the whole row; the row is in L2).  Spreading a row over several CTAs,
+// and a 32-element block over 8 lanes, shortens the splits' serial per-block steps.
+constexpr int RMS_THREADS = 256;
+constexpr int RMS_COLS = RMS_THREADS * 4;  // output columns per CTA
+constexpr int RMS_CHUNKS = 4;  // 8-element chunks per thread of the sum: rows up to 8192 wide
 
-// Output chunk q (elements 8q .. 8q + 7) of row r: v = bf16(x * inv * gamma) stored as its
-// f16 copy, plus the optional e2m1 term split and e4m3 hi/lo split of v.  Every lane of the
-// warp calls it (the splits' block maxima are shuffles).  Not inlined, so that the kernel's
-// call before griddepcontrol.wait (live false: nothing is stored) brings exactly this code
-// into the instruction caches: the kernel runs once per step and its code is otherwise cold.
-__device__ __noinline__ void rms_out_chunk(const NormArgs& a, int r, int q, uint4 xq, uint4 gq,
-                                           float inv, bool live) {
-  const int i = q * 8;
+__device__ __forceinline__ void bf16x4_to_f32(uint2 v, float (&f)[4]) {
+  f[0] = __uint_as_float(v.x << 16), f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(v.y << 16), f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+}
+
+// Output elements i = 4q .. 4q + 3 of row r: v = bf16(x * inv * gamma) stored as its f16 copy,
+// plus the optional e2m1 term split and e4m3 hi/lo split of v.  Every lane of the warp calls
+// it (the splits' block maxima are shuffles).  Not inlined, so that the kernel's call before
+// griddepcontrol.wait (live false: nothing is stored) brings exactly this code into the
+// instruction caches: the kernel runs once per step and its code is otherwise cold.
+__device__ __noinline__ void rms_out4(const NormArgs& a, int r, int q, uint2 xq, uint2 gq,
+                                      float inv, bool live) {
+  const int i = q * 4;
   const bool in = live && i < a.dim;
-  float v[8];
+  float v[4];
   {
-    float f[8], g[8];
-    bf16x8_to_f32(xq, f);
-    bf16x8_to_f32(gq, g);
+    float f[4], g[4];
+    bf16x4_to_f32(xq, f);
+    bf16x4_to_f32(gq, g);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = in ? round_bf16(f[j] * inv * g[j]) : 0.0f;
+    for (int j = 0; j < 4; ++j) v[j] = in ? round_bf16(f[j] * inv * g[j]) : 0.0f;
   }
-  if (in) {
-    uint4 o;
-    o.x = pack_f16x2_sat(v[0], v[1], a.status);
-    o.y = pack_f16x2_sat(v[2], v[3], a.status);
-    o.z = pack_f16x2_sat(v[4], v[5], a.status);
-    o.w = pack_f16x2_sat(v[6], v[7], a.status);
-    *reinterpret_cast<uint4*>(a.out + (size_t)r * a.out_ld + i) = o;
-  }
-  if (a.terms) {  // (a whole warp's chunks are in range or out of it: dim % 256 == 0)
+  if (in)
+    *reinterpret_cast<uint2*>(a.out + (size_t)r * a.out_ld + i) =
+        make_uint2(pack_f16x2_sat(v[0], v[1], a.status), pack_f16x2_sat(v[2], v[3], a.status));
+  if (a.terms) {  // (a whole warp's elements are in range or out of it: dim % 256 == 0)
     uint32_t words[ACT_TERMS], codes[ACT_TERMS];
-    split_terms_x8(v, words, codes);
+    split_terms_x4(v, words, codes);
     if (in) {
-      const int piece = (q & 31) >> 2;  // 16-byte piece (= 32-element block) in its row
-      const size_t base = ((size_t)r * (a.dim / 256) + (q >> 5)) * ACT_TERMS;
+      const int piece = (i & 255) >> 5;  // 16-byte piece (= 32-element block) in its row
+      const size_t base = ((size_t)r * (a.dim / 256) + (i >> 8)) * ACT_TERMS;
 #pragma unroll
       for (int t = 0; t < ACT_TERMS; ++t) {
-        *reinterpret_cast<uint32_t*>(a.terms + (base + t) * 128 + ((piece ^ t) << 4) +
-                                     (q & 3) * 4) = words[t];
-        if ((q & 3) == 0) a.term_scales[(base + t) * 8 + piece] = (uint8_t)codes[t];
+        *reinterpret_cast<uint16_t*>(a.terms + (base + t) * 128 + ((piece ^ t) << 4) +
+                                     ((i & 31) >> 1)) = (uint16_t)words[t];
+        if ((i & 31) == 0) a.term_scales[(base + t) * 8 + piece] = (uint8_t)codes[t];
       }
     }
   }
-  if (a.e4_data) split_store8(v, in, r, i, a.e4_data, a.e4_img);
+  if (a.e4_data) split_store4(v, in, r, i, a.e4_data, a.e4_img);
 }
 
 __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_kernel(const __grid_constant__ NormArgs a) {
   __shared__ float red[32];
   pdl_trigger();
-  const int r = blockIdx.x, tid = threadIdx.x, y = blockIdx.y;
-  const int q = y * RMS_THREADS + tid;  // this thread's output chunk
+  const int r = blockIdx.x, tid = threadIdx.x;
+  const int q = blockIdx.y * RMS_THREADS + tid;  // this thread's 4 output elements
+  const bool mine_in = q * 4 < a.dim;
   const __nv_bfloat16* x = a.in + (size_t)r * a.in_ld;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  const uint2 zero2 = make_uint2(0u, 0u);
   // gamma is constant: fetched before the wait (with the warm-up of the output code)
-  const uint4 gq = q * 8 < a.dim ? *reinterpret_cast<const uint4*>(a.gamma + q * 8) : zero;
-  if (a.warm) rms_out_chunk(a, r, q, zero, zero, 0.0f, false);
+  const uint2 gq = mine_in ? *reinterpret_cast<const uint2*>(a.gamma + q * 4) : zero2;
+  if (a.warm) rms_out4(a, r, q, zero2, zero2, 0.0f, false);
   pdl_wait();
+  // the whole row in 8-element chunks for the sum, and this thread's own 4 elements
   uint4 xv[RMS_CHUNKS], rv[RMS_CHUNKS];
 #pragma unroll
   for (int c = 0; c < RMS_CHUNKS; ++c) {
     const int i = (c * RMS_THREADS + tid) * 8;
     xv[c] = i < a.dim ? *reinterpret_cast<const uint4*>(x + i) : zero;
   }
+  uint2 mine = mine_in ? *reinterpret_cast<const uint2*>(x + q * 4) : zero2;
   if (a.resid) {
     // residual first: h = bf16(x + resid).  The f32 sum of two bf16 values rounds to the
     // same bf16 as their exact sum (an f32 rounding error only arises when the exponents
@@ -90,6 +95,7 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_kernel(const __grid_const
       const int i = (c * RMS_THREADS + tid) * 8;
       rv[c] = i < a.dim ? *reinterpret_cast<const uint4*>(rr + i) : zero;
     }
+    const uint2 rmine = mine_in ? *reinterpret_cast<const uint2*>(rr + q * 4) : zero2;
 #pragma unroll
     for (int c = 0; c < RMS_CHUNKS; ++c) {
       float f[8], g[8];
@@ -100,22 +106,23 @@ __global__ void __launch_bounds__(RMS_THREADS) rmsnorm_kernel(const __grid_const
       xv[c].z = pack_bf16x2(f[4] + g[4], f[5] + g[5]);
       xv[c].w = pack_bf16x2(f[6] + g[6], f[7] + g[7]);
     }
+    float f[4], g[4];
+    bf16x4_to_f32(mine, f);
+    bf16x4_to_f32(rmine, g);
+    mine = make_uint2(pack_bf16x2(f[0] + g[0], f[1] + g[1]), pack_bf16x2(f[2] + g[2], f[3] + g[3]));
+    if (mine_in) *reinterpret_cast<uint2*>(a.sum_out + (size_t)r * a.sum_ld + q * 4) = mine;
   }
   float ss = 0.0f;
-  uint4 mine = zero;  // chunk q of the row (h, when the residual is added)
 #pragma unroll
   for (int c = 0; c < RMS_CHUNKS; ++c) {
     float f[8];
     bf16x8_to_f32(xv[c], f);  // (zero past the row's end)
 #pragma unroll
     for (int j = 0; j < 8; ++j) ss = fmaf(f[j], f[j], ss);
-    if (c == y) mine = xv[c];
   }
-  if (a.resid && q * 8 < a.dim)
-    *reinterpret_cast<uint4*>(a.sum_out + (size_t)r * a.sum_ld + q * 8) = mine;
   ss = block_sum(ss, red);
   const float inv = 1.0f / sqrtf(ss / (float)a.dim + a.eps);
-  rms_out_chunk(a, r, q, mine, gq, inv, true);
+  rms_out4(a, r, q, mine, gq, inv, true);
 }
 
 // Physical page of token t of request q, or -1 when the block table does not map it.
@@ -299,8 +306,8 @@ __global__ void __launch_bounds__(FINAL_THREADS) final_kernel(FinalArgs a) {
 }  // namespace
 
 cudaError_t launch_rmsnorm(const Launch& L, const NormArgs& a, int rows) {
-  if (a.dim > RMS_CHUNKS * RMS_THREADS * 8) return cudaErrorInvalidValue;
-  const int slices = (a.dim + RMS_THREADS * 8 - 1) / (RMS_THREADS * 8);
+  if (a.dim > RMS_CHUNKS * RMS_THREADS * 8 || a.dim % 8) return cudaErrorInvalidValue;
+  const int slices = (a.dim + RMS_COLS - 1) / RMS_COLS;
   return launch_ex(L, dim3(rows, slices), dim3(RMS_THREADS), 0, rmsnorm_kernel, a);
 }
 
