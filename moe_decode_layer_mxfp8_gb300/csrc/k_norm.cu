@@ -137,74 +137,83 @@ __device__ __forceinline__ int page_of(const int* table, int max_blocks, int n_r
 // q-norm and kv-norm of one row, then the fp8 KV insert of the normed kv at the row's
 // position: s = amax / 448 (1 when amax = 0), codes = e4m3(kv / s) rounded to nearest even
 // and saturating, record = codes then s as f32.  Pad rows (position < 0) insert nothing.
-// Thread t owns q chunk t (and t + 256, ...) and kv chunk t: 8 values each.
+// The two norms are independent: CTA (row, 0) normalises q (thread t owns q chunks t,
+// t + 256, ...: 8 values each) and CTA (row, 1) kv (thread t owns kv chunk t) and inserts it.
 constexpr int QKV_CHUNKS = 2;  // q latents up to 4096 wide
 __global__ void __launch_bounds__(NORM_THREADS) qkv_norm_insert_kernel(QkvNormInsertArgs a) {
   __shared__ float red[32];
   pdl_trigger();
   const int r = blockIdx.x, tid = threadIdx.x;
   const __nv_bfloat16* row = a.qkv + (size_t)r * (a.q_rank + a.kv_dim);
-  const bool has_kv = tid * 8 < a.kv_dim;  // kv_dim <= 1024: one chunk per thread at most
-  uint4 qv[QKV_CHUNKS], qg[QKV_CHUNKS], kv = {}, kg = {};
-  // the gammas and the step's inputs (position, page table) before the wait
+  if (blockIdx.y == 0) {
+    // ------------------------------------------------------------------------ q norm
+    uint4 qv[QKV_CHUNKS], qg[QKV_CHUNKS];
 #pragma unroll
-  for (int c = 0; c < QKV_CHUNKS; ++c) {
-    const int i = (c * NORM_THREADS + tid) * 8;
-    if (i < a.q_rank) qg[c] = *reinterpret_cast<const uint4*>(a.gq + i);
+    for (int c = 0; c < QKV_CHUNKS; ++c) {  // gamma before the wait
+      const int i = (c * NORM_THREADS + tid) * 8;
+      if (i < a.q_rank) qg[c] = *reinterpret_cast<const uint4*>(a.gq + i);
+    }
+    pdl_wait();
+#pragma unroll
+    for (int c = 0; c < QKV_CHUNKS; ++c) {
+      const int i = (c * NORM_THREADS + tid) * 8;
+      if (i < a.q_rank) qv[c] = *reinterpret_cast<const uint4*>(row + i);
+    }
+    float ssq = 0.0f;
+#pragma unroll
+    for (int c = 0; c < QKV_CHUNKS; ++c) {
+      if ((c * NORM_THREADS + tid) * 8 < a.q_rank) {
+        float f[8];
+        bf16x8_to_f32(qv[c], f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ssq = fmaf(f[j], f[j], ssq);
+      }
+    }
+    ssq = block_sum(ssq, red);
+    const float invq = 1.0f / sqrtf(ssq / (float)a.q_rank + a.eps);
+#pragma unroll
+    for (int c = 0; c < QKV_CHUNKS; ++c) {
+      const int i = (c * NORM_THREADS + tid) * 8;
+      const bool in = i < a.q_rank;
+      float v[8];
+      if (in) {
+        float f[8], g[8];
+        bf16x8_to_f32(qv[c], f);
+        bf16x8_to_f32(qg[c], g);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = round_bf16(f[j] * invq * g[j]);
+        uint4 o;
+        o.x = pack_f16x2_sat(v[0], v[1], a.status);
+        o.y = pack_f16x2_sat(v[2], v[3], a.status);
+        o.z = pack_f16x2_sat(v[4], v[5], a.status);
+        o.w = pack_f16x2_sat(v[6], v[7], a.status);
+        *reinterpret_cast<uint4*>(a.qlatn + (size_t)r * a.q_rank + i) = o;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+      }
+      if (a.e4_data) split_store8(v, in, r, i, a.e4_data, a.e4_img);  // (every lane)
+    }
+    return;
   }
+  // ------------------------------------------------------------------ kv norm, insert
+  const bool has_kv = tid * 8 < a.kv_dim;  // kv_dim <= 2048: one chunk per thread at most
+  uint4 kv = {}, kg = {};
+  // the gamma and the step's inputs (position, page table) before the wait
   if (has_kv) kg = *reinterpret_cast<const uint4*>(a.gkv + tid * 8);
   const int p = a.positions[r];
   const int pb = p < 0 ? -1 : page_of(a.block_table, a.max_blocks, a.n_req, a.num_blocks,
                                      a.row_req[r], p, a.block_size);
   pdl_wait();
-#pragma unroll
-  for (int c = 0; c < QKV_CHUNKS; ++c) {
-    const int i = (c * NORM_THREADS + tid) * 8;
-    if (i < a.q_rank) qv[c] = *reinterpret_cast<const uint4*>(row + i);
-  }
   if (has_kv) kv = *reinterpret_cast<const uint4*>(row + a.q_rank + tid * 8);
-  float ssq = 0.0f, sskv = 0.0f;
-#pragma unroll
-  for (int c = 0; c < QKV_CHUNKS; ++c) {
-    if ((c * NORM_THREADS + tid) * 8 < a.q_rank) {
-      float f[8];
-      bf16x8_to_f32(qv[c], f);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) ssq = fmaf(f[j], f[j], ssq);
-    }
-  }
+  float sskv = 0.0f;
   float kf[8];
   bf16x8_to_f32(kv, kf);
   if (has_kv)
 #pragma unroll
     for (int j = 0; j < 8; ++j) sskv = fmaf(kf[j], kf[j], sskv);
-  ssq = block_sum(ssq, red);
   sskv = block_sum(sskv, red);
-  const float invq = 1.0f / sqrtf(ssq / (float)a.q_rank + a.eps);
   const float invkv = 1.0f / sqrtf(sskv / (float)a.kv_dim + a.eps);
-#pragma unroll
-  for (int c = 0; c < QKV_CHUNKS; ++c) {
-    const int i = (c * NORM_THREADS + tid) * 8;
-    const bool in = i < a.q_rank;
-    float v[8];
-    if (in) {
-      float f[8], g[8];
-      bf16x8_to_f32(qv[c], f);
-      bf16x8_to_f32(qg[c], g);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = round_bf16(f[j] * invq * g[j]);
-      uint4 o;
-      o.x = pack_f16x2_sat(v[0], v[1], a.status);
-      o.y = pack_f16x2_sat(v[2], v[3], a.status);
-      o.z = pack_f16x2_sat(v[4], v[5], a.status);
-      o.w = pack_f16x2_sat(v[6], v[7], a.status);
-      *reinterpret_cast<uint4*>(a.qlatn + (size_t)r * a.q_rank + i) = o;
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
-    }
-    if (a.e4_data) split_store8(v, in, r, i, a.e4_data, a.e4_img);  // (every lane)
-  }
   float kn[8], g[8];
   bf16x8_to_f32(kg, g);
   float amax = 0.0f;
@@ -312,7 +321,9 @@ cudaError_t launch_rmsnorm(const Launch& L, const NormArgs& a, int rows) {
 }
 
 cudaError_t launch_qkv_norm_insert(const Launch& L, const QkvNormInsertArgs& a, int rows) {
-  return launch_ex(L, dim3(rows), dim3(NORM_THREADS), 0, qkv_norm_insert_kernel, a);
+  if (a.q_rank > QKV_CHUNKS * NORM_THREADS * 8 || a.kv_dim > NORM_THREADS * 8)
+    return cudaErrorInvalidValue;
+  return launch_ex(L, dim3(rows, 2), dim3(NORM_THREADS), 0, qkv_norm_insert_kernel, a);
 }
 
 cudaError_t launch_final(const Launch& L, const FinalArgs& a) {
