@@ -17,7 +17,7 @@
 // epilogue.  (A CTA's stage costs some 900 cycles of issue and bookkeeping across its two
 // pipeline warps, so one pipeline per SM falls short of the SM's share of HBM bandwidth; two
 // reach it.)  Items are (hit expert, group of up to 8 routed rows, weight tile), handed out
-// by a per-launch counter, largest groups first.
+// by a per-launch counter, largest groups first (the order the top-k publishes).
 // gate_up tiles are 64 gate rows with the 64 up rows they pair with; the epilogue forms
 // SwiGLU and writes t (f16) and t's term split for the down GEMM.  Every wait is bounded.
 #include <algorithm>
