@@ -637,7 +637,7 @@ def _workload_desc(name, spec, rows):
 # kernel, from an ncu capture of one launch, keyed by the md5 of the kernel's sources it was
 # taken on: reported only while those are unchanged.
 NCU_TRAFFIC = {
-    ("full_r48", "expert_gate_up"): (503_944_448, "e6691b8db334c81af54039c077f18b00"
+    ("full_r48", "expert_gate_up"): (503_944_448, "2472908a64ea93377cde950225ba4334"
                                                   "06e4e11ed408713cfcd80ad3695d0c0c"
                                                   "be64dae3d39c85a34e55a21d81c7b9b0"),
 }
