@@ -18,7 +18,7 @@ namespace mono {
 
 namespace {
 
-constexpr int ATTN_THREADS = 256;  // 8 warps
+constexpr int ATTN_THREADS = 512;  // 16 warps: one 8-key score tile, head or 8-dim output tile each
 constexpr int ATTN_KEYS = 128;     // keys per split at most
 constexpr int ATTN_HEADS = 16;     // heads per latent slice at most (= the MMA's M)
 
