@@ -120,16 +120,19 @@ struct Pick {
   float sum;  // the sum of exp(z - z_max) over the row's k picks
 };
 
-// Top-k of one row of logits by a group of lpr lanes (8 for E <= 128, 16 for E <= 256), 16
-// logits per lane packed with their expert index as (order key << 32 | 255 - e): the
-// largest packed value is the largest logit, ties to the lowest expert index; k rounds of a
-// local max and a butterfly over the group.  Not inlined, so that the kernel's call before
-// griddepcontrol.wait (on no data, with live false) brings exactly this code into the
-// instruction caches: the kernel runs once per step and its code is otherwise cold.
+// Top-k of one row of logits by a group of lpr lanes, VPL logits per lane (lpr * VPL >= E:
+// 8 x 16 for E <= 128 or 16 x 16 for E <= 256 when a warp takes several rows; a whole warp,
+// 32 x 4 or 32 x 8, when the step has at most one row per warp), each packed with its expert
+// index as (order key << 32 | 255 - e): the largest packed value is the largest logit, ties
+// to the lowest expert index; k rounds of a local max and a butterfly over the group.  Not
+// inlined, so that the kernel's call before griddepcontrol.wait (on no data, with live false)
+// brings exactly this code into the instruction caches: the kernel runs once per step and its
+// code is otherwise cold.
+template <int VPL>
 __device__ __noinline__ Pick select_topk(const float* z, int E, int k, int lpr, int li, bool live) {
-  unsigned long long pv[16];
+  unsigned long long pv[VPL];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
+  for (int j = 0; j < VPL; ++j) {
     const int e = li + lpr * j;
     pv[j] = live && e < E ? ((unsigned long long)order_key(z[e] + 0.0f) << 32) |
                                 (unsigned long long)(255 - e)
@@ -141,7 +144,7 @@ __device__ __noinline__ Pick select_topk(const float* z, int E, int k, int lpr, 
   for (int kk = 0; kk < k; ++kk) {
     unsigned long long b = 0ull;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) b = max(b, pv[j]);
+    for (int j = 0; j < VPL; ++j) b = max(b, pv[j]);
     for (int o = 1; o < lpr; o <<= 1) b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
     const int be = 255 - (int)(b & 0xFFull);
     const float bv = key_value((uint32_t)(b >> 32));
@@ -150,7 +153,7 @@ __device__ __noinline__ Pick select_topk(const float* z, int E, int k, int lpr, 
     pk.sum += ex;
     if (li == kk) pk.ex = ex, pk.e = be;  // lane kk of the group keeps slot kk
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
+    for (int j = 0; j < VPL; ++j)
       if (li + lpr * j == be) pv[j] = 0ull;
   }
   return pk;
@@ -176,8 +179,12 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
   for (int e = tid; e < MAX_EXPERTS; e += TOPK_THREADS) s_mask[e] = 0ull;
   for (int i = tid; i < 64 * (MAX_EXPERTS / 32); i += TOPK_THREADS) (&s_kmask[0][0])[i] = 0u;
   if (tid < a.rows) s_pos[tid] = a.positions[tid];  // a step input: read before the wait
+  // at most one row per warp: a whole warp per row (shorter per-lane chains in each round)
+  const bool wide = a.rows <= NW;
   if (warp == 0) {  // warm the selection code while the previous kernel finishes
-    const Pick dry = select_topk(s_z, a.E, a.k, a.E <= 128 ? 8 : 16, lane & 7, false);
+    const Pick dry = !wide          ? select_topk<16>(s_z, a.E, a.k, a.E <= 128 ? 8 : 16, lane & 7, false)
+                     : a.E <= 128 ? select_topk<4>(s_z, a.E, a.k, 32, lane, false)
+                                  : select_topk<8>(s_z, a.E, a.k, 32, lane, false);
     if (dry.e == -2) s_pos[0] = 0;  // never true: keeps the call
   }
   pdl_wait();
@@ -209,15 +216,18 @@ __global__ void __launch_bounds__(TOPK_THREADS) topk_kernel(TopkArgs a) {
     }
   }
   __syncthreads();
-  // phase 1b: selection, a group of 8 or 16 lanes per row (select_topk)
+  // phase 1b: selection, a group of 8 or 16 lanes per row, or a warp (select_topk)
   {
-    const int lpr = a.E <= 128 ? 8 : 16;
+    const int lpr = wide ? 32 : a.E <= 128 ? 8 : 16;
     const int rpw = 32 / lpr;  // rows per warp
     const int li = lane & (lpr - 1), grp = lane / lpr;
     for (int r0 = warp * rpw; r0 < a.rows; r0 += NW * rpw) {
       const int r = r0 + grp;
       const bool live = r < a.rows;
-      const Pick pk = select_topk(s_z + r * a.E, a.E, a.k, lpr, li, live);
+      const float* zr = s_z + r * a.E;
+      const Pick pk = !wide        ? select_topk<16>(zr, a.E, a.k, lpr, li, live)
+                      : a.E <= 128 ? select_topk<4>(zr, a.E, a.k, lpr, li, live)
+                                   : select_topk<8>(zr, a.E, a.k, lpr, li, live);
       const int my_e = pk.e;
       const float my_ex = pk.ex, ex_sum = pk.sum;
       if (live && li < a.k) {
